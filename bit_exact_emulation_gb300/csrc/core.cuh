@@ -1,0 +1,657 @@
+// core.cuh -- device side of the emulator: input decoding, the multi-term
+// adder architectures of "Accurate Models of AMD Matrix Cores" and the
+// rounding of their integer results to fp32.  Shared by every kernel.
+//
+// Vocabulary (paper notation):  p_l = a_l * b_l is kept as an integer
+// significand product U_l = S_a * S_b with fraction bits m_a + m_b and the
+// denormalised exponent e_l = E_a + E_b (Sec. 4.3.1); c has significand S_c
+// (23 fraction bits) and exponent e_c; e_max is the maximum exponent that the
+// terms are aligned to; F_p the fraction bits kept after alignment.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "model.h"
+
+namespace mcemu {
+
+// ---------------------------------------------------------------------------
+// small integer helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t shr32(uint32_t x, int32_t s) {   // s >= 0, 0 when s >= 32
+  return __funnelshift_rc(x, 0u, (uint32_t)s);
+}
+__device__ __forceinline__ uint64_t shr64(uint64_t x, int32_t s) {   // s >= 0
+  return s >= 64 ? 0ull : (x >> s);
+}
+__device__ __forceinline__ int64_t sar64(int64_t x, int32_t s) {     // floor(x / 2^s), s >= 0
+  return x >> (s > 63 ? 63 : s);
+}
+__device__ __forceinline__ int32_t sar32(int32_t x, int32_t s) {
+  return x >> (s > 31 ? 31 : s);
+}
+
+// ---------------------------------------------------------------------------
+// decoding
+// ---------------------------------------------------------------------------
+// XF32: an fp32 container whose mantissa is reduced to 10 bits (Sec. 4.3.3).
+__device__ __forceinline__ uint32_t xf32_reduce(uint32_t bits, uint32_t mode) {
+  if (mode == 1u) return bits & 0xFFFFE000u;
+  return (bits + 0xFFFu + ((bits >> 13) & 1u)) & 0xFFFFE000u;   // RNE, may carry into Inf
+}
+
+// Finite decode: value = (-1)^neg * S * 2^(E - m_eff).  Zero (and flushed
+// subnormals) give S = 0.  Inf/NaN decode to garbage and are caught apart.
+__device__ __forceinline__ void decode(const FmtDev &f, uint32_t bits, uint32_t &S, int32_t &E,
+                                       uint32_t &neg) {
+  if (f.xf32) bits = xf32_reduce(bits, f.xf32);
+  uint32_t ef = (bits >> f.mbits) & f.emask;
+  uint32_t mf = bits & ((1u << f.mbits) - 1u);
+  neg = (bits >> f.sshift) & 1u;
+  S = (ef ? (mf | (1u << f.mbits)) : (mf & f.sub_keep)) >> f.sig_rshift;
+  E = (int32_t)(ef ? ef : 1u) - f.bias;
+}
+
+// Special-value class of one element: 0 finite, 1 Inf, 2 NaN (sign apart).
+__device__ __forceinline__ uint32_t classify(const FmtDev &f, uint32_t bits) {
+  uint32_t ef = (bits >> f.mbits) & f.emask;
+  uint32_t mf = bits & ((1u << f.mbits) - 1u);
+  if ((bits & f.nan_mask) == f.nan_pat) return 2u;
+  if (ef == f.top_special) {
+    if (mf) return 2u;
+    return 1u;
+  }
+  if (f.xf32 == 2u) {               // RNE reduction can round the largest finites to Inf
+    uint32_t r = xf32_reduce(bits, 2u);
+    if (((r >> 23) & 0xFFu) == 0xFFu) return 1u;
+  }
+  return 0u;
+}
+
+__device__ __forceinline__ bool is_zero_elem(const FmtDev &f, uint32_t bits) {
+  uint32_t S; int32_t E; uint32_t neg;
+  decode(f, bits, S, E, neg);
+  return S == 0u && classify(f, bits) == 0u;
+}
+
+// SWAR test of a 32-bit word of packed elements: nonzero when some element is
+// Inf/NaN (the exponent field all ones carries into the sign position), or, for
+// FNUZ, some byte is 0x80.
+__device__ __forceinline__ uint32_t special_word(const FmtDev &f, uint32_t w) {
+  uint32_t s = ((w & f.sw_mask) + f.sw_add) & f.sw_hi;
+  if (f.sw_fnuz) {
+    uint32_t x = w ^ 0x80808080u;
+    s |= (x - 0x01010101u) & ~x & 0x80808080u;
+  }
+  if (f.xf32 == 2u) s |= ((xf32_reduce(w, 2u) & 0x7F800000u) + 0x00800000u) & 0x80000000u;
+  return s;
+}
+
+// fp32 addend c (always binary32 bits).
+__device__ __forceinline__ void decode_c(const DevModel &m, uint32_t bits, uint32_t &S, int32_t &E,
+                                         uint32_t &neg) {
+  uint32_t ef = (bits >> 23) & 0xFFu;
+  uint32_t mf = bits & 0x7FFFFFu;
+  neg = bits >> 31;
+  S = ef ? (mf | 0x800000u) : (mf & m.c_sub_keep);
+  E = (int32_t)(ef ? ef : 1u) - 127;
+}
+
+// ---------------------------------------------------------------------------
+// special values: every model gives NaN for a NaN input, Inf*0 or Inf-Inf, and
+// the signed Inf otherwise (Secs. 4.1-4.3).  Bits: 1 NaN, 2 +Inf, 4 -Inf.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t product_special(const DevModel &m, uint32_t ab, uint32_t bb) {
+  uint32_t ca = classify(m.fa, ab), cb = classify(m.fb, bb);
+  if (ca == 2u || cb == 2u) return 1u;
+  if (ca == 0u && cb == 0u) return 0u;
+  bool za = (ca == 0u) && is_zero_elem(m.fa, ab);
+  bool zb = (cb == 0u) && is_zero_elem(m.fb, bb);
+  if (za || zb) return 1u;                                    // Inf * 0
+  uint32_t neg = ((ab >> m.fa.sshift) ^ (bb >> m.fb.sshift)) & 1u;
+  return neg ? 4u : 2u;
+}
+
+__device__ __forceinline__ uint32_t c_special(uint32_t cb) {
+  if ((cb & 0x7F800000u) != 0x7F800000u) return 0u;
+  if (cb & 0x7FFFFFu) return 1u;
+  return (cb >> 31) ? 4u : 2u;
+}
+
+__device__ __forceinline__ uint32_t resolve_special(const DevModel &m, uint32_t s) {
+  if ((s & 1u) || (s & 6u) == 6u) return m.nan_bits;
+  return (s & 2u) ? 0x7F800000u : 0xFF800000u;
+}
+
+// ---------------------------------------------------------------------------
+// rounding of an exact (or sticky-carrying) magnitude to fp32
+// value = (-1)^neg * (M + f) * 2^lsb with f in (0,1) when sticky, else f = 0.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t overflow_bits(int rne) {
+  return rne ? 0x7F800000u : 0x7F7FFFFFu;
+}
+
+__device__ __forceinline__ uint32_t round_pack(uint64_t M, int32_t lsb, uint32_t neg, bool sticky,
+                                               int rne, int flush) {
+  // M > 0, M < 2^62
+  int32_t p = 63 - __clzll((long long)M);
+  int32_t E = lsb + p;
+  int32_t Ec = E < -126 ? -126 : E;
+  if (Ec > 127) return overflow_bits(rne) | (neg << 31);
+  int32_t r = Ec - 23 - lsb;                 // bits of M below the fp32 grid
+  uint64_t q;
+  uint32_t up = 0;
+  if (r <= 0) {
+    q = M << (-r);
+  } else if (r > 62) {
+    q = 0;
+  } else {
+    q = M >> r;
+    uint64_t rem = M & ((1ull << r) - 1ull);
+    uint64_t half = 1ull << (r - 1);
+    if (rne) up = (rem > half || (rem == half && (sticky || (q & 1ull)))) ? 1u : 0u;
+  }
+  uint32_t bits = ((uint32_t)(Ec + 126) << 23) + (uint32_t)q + up;
+  if (bits >= 0x7F800000u) bits = overflow_bits(rne);
+  if (flush && bits < 0x00800000u) bits = 0u;
+  return bits | (neg << 31);
+}
+
+// 32-bit fast path: M < 2^31, no sticky.
+__device__ __forceinline__ uint32_t round_pack32(uint32_t M, int32_t lsb, uint32_t neg, int rne,
+                                                 int flush) {
+  int32_t p = 31 - __clz((int)M);
+  int32_t E = lsb + p;
+  int32_t Ec = E < -126 ? -126 : E;
+  if (Ec > 127) return overflow_bits(rne) | (neg << 31);
+  int32_t r = Ec - 23 - lsb;
+  uint32_t q, up = 0;
+  if (r <= 0) {
+    q = M << (-r);
+  } else if (r > 31) {
+    q = 0;
+  } else {
+    q = M >> r;
+    uint32_t rem = M & ((2u << (r - 1)) - 1u);
+    uint32_t half = 1u << (r - 1);
+    if (rne) up = (rem > half || (rem == half && (q & 1u))) ? 1u : 0u;
+  }
+  uint32_t bits = ((uint32_t)(Ec + 126) << 23) + q + up;
+  if (bits >= 0x7F800000u) bits = overflow_bits(rne);
+  if (flush && bits < 0x00800000u) bits = 0u;
+  return bits | (neg << 31);
+}
+
+// ---------------------------------------------------------------------------
+// terms of eq. (1)
+// ---------------------------------------------------------------------------
+template <class UT>
+struct Term {
+  UT U;          // |S_a * S_b|
+  int32_t e;     // E_a + E_b, kNegE for a zero product
+  uint32_t neg;  // 0 / 1
+};
+
+template <class UT>
+__device__ __forceinline__ Term<UT> make_term(const DevModel &m, uint32_t ab, uint32_t bb) {
+  uint32_t Sa, Sb, na, nb;
+  int32_t Ea, Eb;
+  decode(m.fa, ab, Sa, Ea, na);
+  decode(m.fb, bb, Sb, Eb, nb);
+  Term<UT> t;
+  t.U = (UT)Sa * (UT)Sb;
+  t.e = t.U ? Ea + Eb : kNegE;
+  t.neg = na ^ nb;
+  return t;
+}
+
+// CDNA3: |p| >= 2^128 becomes +-Inf (Sec. 4.3.2).  Returns special bits.
+template <class UT>
+__device__ __forceinline__ uint32_t product_overflow(const DevModel &m, const Term<UT> &t) {
+  // |p| = U * 2^(e - mab) >= 2^128  <=>  msb(U) + e - mab >= 128
+  if (!t.U) return 0u;
+  int32_t msb = (sizeof(UT) == 8) ? 63 - __clzll((long long)t.U) : 31 - __clz((int)t.U);
+  if (msb + t.e - m.mab >= 128) return t.neg ? 4u : 2u;
+  return 0u;
+}
+
+// zero result: negative only when every product is a negative zero and c is -0
+template <int K, class UT>
+__device__ __forceinline__ uint32_t zero_result(const Term<UT> (&p)[K], int nt, uint32_t cS,
+                                                uint32_t cneg) {
+  bool all_neg = (cS == 0u) && cneg;
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if (l < nt) all_neg = all_neg && (p[l].U == 0) && p[l].neg;
+  return all_neg ? 0x80000000u : 0u;
+}
+
+// ---------------------------------------------------------------------------
+// aligned, truncated term: RZ or RD of +-U * 2^(F_p - shift) on the integer grid
+// ---------------------------------------------------------------------------
+template <class UT, class AT>
+__device__ __forceinline__ AT align_term(UT Ushift, uint32_t neg, int32_t sh, int rd) {
+  // Ushift = U << P0 (< 2^(width-1)); sh >= 0 is the right shift to the grid.
+  if (sizeof(AT) == 4) {
+    if (rd) {
+      int32_t v = neg ? -(int32_t)Ushift : (int32_t)Ushift;
+      return (AT)sar32(v, sh);
+    }
+    uint32_t t = shr32((uint32_t)Ushift, sh);
+    return (AT)(neg ? -(int32_t)t : (int32_t)t);
+  } else {
+    if (rd) {
+      int64_t v = neg ? -(int64_t)Ushift : (int64_t)Ushift;
+      return (AT)sar64(v, sh);
+    }
+    uint64_t t = shr64((uint64_t)Ushift, sh);
+    return (AT)(neg ? -(int64_t)t : (int64_t)t);
+  }
+}
+
+template <class AT>
+__device__ __forceinline__ uint32_t pack_sum(AT S, int32_t lsb, const DevModel &m) {
+  uint32_t neg = S < 0 ? 1u : 0u;
+  if (sizeof(AT) == 4) {
+    uint32_t M = neg ? (uint32_t)(-(int32_t)S) : (uint32_t)S;
+    return round_pack32(M, lsb, neg, m.rne, m.sub_out_flush);
+  }
+  uint64_t M = neg ? (uint64_t)(-(int64_t)S) : (uint64_t)S;
+  return round_pack(M, lsb, neg, false, m.rne, m.sub_out_flush);
+}
+
+// ---------------------------------------------------------------------------
+// GA_EARLY: global alignment with c aligned together with the products
+// (Table 3, early c; e_{c=0} and e_min^lim as configured).
+// ---------------------------------------------------------------------------
+template <int K, class UT, class AT>
+__device__ __forceinline__ uint32_t arch_ga_early(const DevModel &m, const Term<UT> (&p)[K], int nt,
+                                                  uint32_t cS, int32_t cE, uint32_t cneg) {
+  int32_t emax = m.emin_lim;
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if (l < nt) emax = max(emax, p[l].e);
+  int32_t ec = cS ? cE : m.c_zero_exp;
+  emax = max(emax, ec);
+  AT S = 0;
+  const int32_t base = emax + m.R0;
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if (l < nt) S += align_term<UT, AT>(p[l].U << m.P0, p[l].neg, base - p[l].e, m.align_rd);
+  if (cS) S += align_term<UT, AT>((UT)cS << m.P0c, cneg, emax + m.R0c - cE, m.align_rd);
+  if (S == 0) return zero_result<K, UT>(p, nt, cS, cneg);
+  return pack_sum<AT>(S, emax - m.F, m);
+}
+
+// ---------------------------------------------------------------------------
+// Late c merge: lines 5-15 of Algorithm 1 (lines 9-20 of Algorithm 2, which
+// also drops a c shifted by more than 25 places: zero_cut).  Sp is the aligned
+// product sum in units of 2^(emax - F_p).
+// ---------------------------------------------------------------------------
+template <int K, class UT, class AT>
+__device__ __forceinline__ uint32_t late_c_merge(const DevModel &m, AT Sp, bool have_p, int32_t emax,
+                                                 const Term<UT> (&p)[K], int nt, uint32_t cS,
+                                                 int32_t cE, uint32_t cneg, bool zero_cut) {
+  int32_t ec = cS ? cE : m.c_zero_exp;      // line 5: e_c = -126 if c = 0
+  bool have_c = ec > kNegE / 2;
+  if (!have_p && !have_c) return zero_result<K, UT>(p, nt, cS, cneg);
+  if (have_p && (!have_c || emax >= ec)) {
+    // line 7: shift s_c right by e_max - e_c, RD to c_frac fraction bits (= F_p)
+    int64_t sc = 0;
+    if (cS && !(zero_cut && emax - ec > 25)) {
+      int64_t v = cneg ? -(int64_t)cS : (int64_t)cS;
+      int32_t sh = emax - ec + 23 - m.c_frac;
+      sc = sh >= 0 ? sar64(v, sh) : v * ((int64_t)1 << (-sh));
+    }
+    int64_t Sacc = (int64_t)Sp + sc;        // line 8
+    if (Sacc == 0) return zero_result<K, UT>(p, nt, cS, cneg);
+    uint32_t neg = Sacc < 0 ? 1u : 0u;
+    uint64_t M = neg ? (uint64_t)(-Sacc) : (uint64_t)Sacc;
+    return round_pack(M, emax - m.F, neg, false, m.rne, m.sub_out_flush);   // line 15
+  }
+  // line 10: shift S_p right by e_c - e_max, RD to psum_frac fraction bits
+  int64_t Sp2 = 0;
+  if (have_p) {
+    int32_t sh = ec - emax - (m.psum_frac - m.F);
+    Sp2 = sh >= 0 ? sar64((int64_t)Sp, sh) : (int64_t)Sp * ((int64_t)1 << (-sh));
+  }
+  // line 11: S_acc = S'_p + s_c on the 2^(e_c - psum_frac) grid
+  int64_t vc = cneg ? -(int64_t)cS : (int64_t)cS;
+  int64_t Sacc = Sp2 + vc * ((int64_t)1 << (m.psum_frac - 23));
+  if (Sacc == 0) return zero_result<K, UT>(p, nt, cS, cneg);
+  uint32_t neg = Sacc < 0 ? 1u : 0u;
+  uint64_t M = neg ? (uint64_t)(-Sacc) : (uint64_t)Sacc;
+  int32_t lsb = ec - m.psum_frac;
+  // line 12: normalise, exponent floored at -126 (subnormal-aware)
+  int32_t E = 63 - __clzll((long long)M) + lsb;
+  if (E < -126) E = -126;
+  // line 13: RD to post_norm_frac fraction bits of the normalised value
+  int32_t r = E - m.post_norm_frac - lsb;
+  if (r > 0) {
+    M = neg ? ((M + ((1ull << r) - 1ull)) >> r) : (M >> r);   // floor of the signed value
+    lsb += r;
+  }
+  return round_pack(M, lsb, neg, false, m.rne, m.sub_out_flush);   // line 15
+}
+
+// Algorithm 1 (CDNA 3 fp16/bf16/tf19): lines 3-4 then the late-c merge.
+template <int K, class UT, class AT>
+__device__ __forceinline__ uint32_t arch_ga_late(const DevModel &m, const Term<UT> (&p)[K], int nt,
+                                                 uint32_t cS, int32_t cE, uint32_t cneg) {
+  int32_t emax = kNegE;                     // line 3
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if (l < nt) emax = max(emax, p[l].e);
+  bool have_p = emax > kNegE / 2;
+  AT Sp = 0;                                // line 4
+  const int32_t base = emax + m.R0;
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if (l < nt) Sp += align_term<UT, AT>(p[l].U << m.P0, p[l].neg, base - p[l].e, m.align_rd);
+  return late_c_merge<K, UT, AT>(m, Sp, have_p, emax, p, nt, cS, cE, cneg, false);
+}
+
+// Algorithm 2 (CDNA 3 binary8): odd (p_1, p_3, ...) and even (p_2, p_4, ...)
+// products aligned to their own maxima (lines 3-5), shifted to the common e_max
+// with RD (lines 6-8), then the late-c merge with the 25-place cut.
+template <int K, class UT, class AT>
+__device__ __forceinline__ uint32_t arch_odd_even(const DevModel &m, const Term<UT> (&p)[K], int nt,
+                                                  uint32_t cS, int32_t cE, uint32_t cneg) {
+  int32_t em0 = kNegE, em1 = kNegE;
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if (l < nt) {
+      if ((l & 1) == 0) em0 = max(em0, p[l].e);
+      else em1 = max(em1, p[l].e);
+    }
+  AT S0 = 0, S1 = 0;
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if (l < nt) {
+      if ((l & 1) == 0) S0 += align_term<UT, AT>(p[l].U << m.P0, p[l].neg, em0 + m.R0 - p[l].e, m.align_rd);
+      else S1 += align_term<UT, AT>(p[l].U << m.P0, p[l].neg, em1 + m.R0 - p[l].e, m.align_rd);
+    }
+  int32_t emax = max(em0, em1);
+  bool have_p = emax > kNegE / 2;
+  AT Sp = 0;
+  if (have_p) {
+    if (em0 > kNegE / 2) Sp += (AT)sar64((int64_t)S0, emax - em0);
+    if (em1 > kNegE / 2) Sp += (AT)sar64((int64_t)S1, emax - em1);
+  }
+  return late_c_merge<K, UT, AT>(m, Sp, have_p, emax, p, nt, cS, cE, cneg, true);
+}
+
+// ---------------------------------------------------------------------------
+// EXACT: correct rounding of the exact sum (CDNA 1).  A 128-bit window anchored
+// at the largest term holds every term that fits; terms reaching below it are
+// floored into it and counted.  The true value then lies in (W, W + nb) units
+// of the window LSB; when both ends round alike that is the answer, otherwise
+// a full-width exact accumulation decides (rare).
+// ---------------------------------------------------------------------------
+typedef __int128 i128;
+typedef unsigned __int128 u128;
+
+__device__ __forceinline__ uint32_t round_pack128(i128 W, int32_t L, bool sticky, const DevModel &m) {
+  uint32_t neg = W < 0 ? 1u : 0u;
+  u128 Mag = neg ? (sticky ? (u128)(~W) : (u128)(-W)) : (u128)W;
+  uint64_t hi = (uint64_t)(Mag >> 64), lo = (uint64_t)Mag;
+  int32_t p = hi ? 127 - __clzll((long long)hi) : (lo ? 63 - __clzll((long long)lo) : -1);
+  if (p < 0) return 0u;                     // not reached: the window sum is never empty
+  int32_t s = p > 61 ? p - 61 : 0;
+  uint64_t M = (uint64_t)(Mag >> s);
+  bool st = sticky || (s > 0 && (Mag & (((u128)1 << s) - 1)) != 0);
+  return round_pack(M, L + s, neg, st, m.rne, m.sub_out_flush);
+}
+
+// full-width exact sum: 32-bit digits in signed 64-bit slots covering 2^-320 .. 2^320
+static __device__ __noinline__ uint32_t exact_slow(const DevModel &m, const int64_t *V, const int32_t *lsb, int nterm) {
+  constexpr int kBase = -320, kDig = 20;
+  int64_t acc[kDig];
+#pragma unroll
+  for (int i = 0; i < kDig; i++) acc[i] = 0;
+  for (int t = 0; t < nterm; t++) {
+    if (V[t] == 0) continue;
+    // split |V| < 2^49 into 24-bit pieces so that piece << 31 fits a slot
+    int64_t v = V[t];
+    int64_t vlo = v & 0xFFFFFF;             // two's complement: v = vhi * 2^24 + vlo
+    int64_t vhi = v >> 24;
+    for (int h = 0; h < 2; h++) {
+      int64_t piece = h ? vhi : vlo;
+      if (!piece) continue;
+      int32_t pos = lsb[t] + 24 * h - kBase;
+      acc[pos >> 5] += piece * ((int64_t)1 << (pos & 31));
+    }
+  }
+  int64_t carry = 0;
+  uint32_t dig[kDig];
+  for (int i = 0; i < kDig; i++) {
+    int64_t x = acc[i] + carry;
+    dig[i] = (uint32_t)x;
+    carry = x >> 32;                        // arithmetic: floor
+  }
+  bool neg = carry < 0;
+  if (neg) {                                // magnitude = two's complement negation
+    uint32_t c1 = 1;
+    for (int i = 0; i < kDig; i++) {
+      uint64_t x = (uint64_t)(~dig[i]) + c1;
+      dig[i] = (uint32_t)x;
+      c1 = (uint32_t)(x >> 32);
+    }
+  }
+  int top = -1;
+  for (int i = kDig - 1; i >= 0; i--)
+    if (dig[i]) { top = i; break; }
+  if (top < 0) return 0u;                   // exact zero: caller handles the sign
+  // gather 64 bits below the top digit boundary, the rest as sticky
+  uint64_t M = ((uint64_t)dig[top] << 32) | (top > 0 ? dig[top - 1] : 0u);
+  bool sticky = false;
+  for (int i = 0; i < top - 1; i++) sticky = sticky || dig[i] != 0;
+  int32_t lsb0 = kBase + 32 * (top - 1);
+  int32_t p = 63 - __clzll((long long)M);
+  if (p > 61) {
+    int s = p - 61;
+    sticky = sticky || (M & ((1ull << s) - 1ull)) != 0;
+    M >>= s;
+    lsb0 += s;
+  }
+  return round_pack(M, lsb0, neg ? 1u : 0u, sticky, m.rne, m.sub_out_flush);
+}
+
+template <int K, class UT>
+__device__ __forceinline__ uint32_t arch_exact(const DevModel &m, const Term<UT> (&p)[K], int nt,
+                                               uint32_t cS, int32_t cE, uint32_t cneg) {
+  int32_t T = kNegE;                        // bound on the top bit of every term
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if (l < nt) T = max(T, p[l].e + 2);
+  if (cS) T = max(T, cE + 1);
+  if (T <= kNegE / 2) return zero_result<K, UT>(p, nt, cS, cneg);
+  const int32_t L = T - 121;
+  i128 W = 0;
+  int32_t nb = 0;
+#pragma unroll
+  for (int l = 0; l <= K; l++) {
+    int64_t v;
+    int32_t lsb;
+    if (l < K) {
+      if (l >= nt) continue;
+      v = p[l].neg ? -(int64_t)p[l].U : (int64_t)p[l].U;
+      lsb = p[l].e - m.mab;
+    } else {
+      v = cneg ? -(int64_t)cS : (int64_t)cS;
+      lsb = cE - 23;
+    }
+    if (v == 0) continue;
+    int32_t sh = lsb - L;
+    if (sh >= 0) {
+      W += (i128)((u128)(i128)v << sh);
+    } else {
+      int32_t s = -sh;
+      if (s >= 63) {
+        W += (v < 0) ? -1 : 0;
+        nb += 1;
+      } else {
+        W += (i128)(v >> s);
+        nb += (v & ((1ll << s) - 1)) != 0;
+      }
+    }
+  }
+  if (nb == 0) {
+    if (W == 0) return zero_result<K, UT>(p, nt, cS, cneg);
+    return round_pack128(W, L, false, m);
+  }
+  uint32_t lo = round_pack128(W, L, true, m);
+  uint32_t hi = round_pack128(W + (nb - 1), L, true, m);
+  if (lo == hi) return lo;
+  int64_t V[K + 1];
+  int32_t Ls[K + 1];
+  int n = 0;
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if (l < nt) {
+      V[n] = p[l].neg ? -(int64_t)p[l].U : (int64_t)p[l].U;
+      Ls[n] = p[l].e - m.mab;
+      n++;
+    }
+  V[n] = cneg ? -(int64_t)cS : (int64_t)cS;
+  Ls[n] = cE - 23;
+  n++;
+  uint32_t r = exact_slow(m, V, Ls, n);
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// PAIRWISE: fl(c + fl(fl(p1+p2) + fl(p3+p4))), fl = RNE to fp32 with optional
+// subnormal flush after every operation (Sec. 4.2).  IEEE fp32 hardware
+// arithmetic is exactly fl() here: the inputs are exact in fp32.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float fl_flush(float x, int flush) {
+  if (flush && fabsf(x) < 1.17549435e-38f) return copysignf(0.0f, x);
+  return x;
+}
+
+// fp32 bits of the exact value (-1)^neg * S * 2^lsb (exact for every input format)
+__device__ __forceinline__ uint32_t exact_fp32_bits(uint32_t S, int32_t lsb, uint32_t neg) {
+  if (!S) return neg << 31;
+  int32_t p = 31 - __clz((int)S);
+  int32_t E = lsb + p;
+  uint32_t bits;
+  if (E >= -126) bits = ((uint32_t)(E + 127) << 23) | ((S << (31 - p)) >> 8 & 0x7FFFFFu);
+  else bits = S << (lsb + 149);            // subnormal: S * 2^(lsb + 149) on the 2^-149 grid
+  return bits | (neg << 31);
+}
+
+__device__ __forceinline__ float elem_to_float(const FmtDev &f, uint32_t bits) {
+  uint32_t cls = classify(f, bits);
+  uint32_t sign = ((bits >> f.sshift) & 1u) << 31;
+  if (cls == 2u) return __uint_as_float(0x7FC00000u);
+  if (cls == 1u) return __uint_as_float(sign | 0x7F800000u);
+  uint32_t S, neg;
+  int32_t E;
+  decode(f, bits, S, E, neg);
+  return __uint_as_float(exact_fp32_bits(S, E - f.m_eff, neg));
+}
+
+template <int K>
+__device__ __forceinline__ uint32_t arch_pairwise(const DevModel &m, const uint32_t (&ab)[K],
+                                                  const uint32_t (&bb)[K], int nt, uint32_t cbits) {
+  float v[K];
+#pragma unroll
+  for (int l = 0; l < K; l++) {
+    if (l < nt) {
+      float x = elem_to_float(m.fa, ab[l]);
+      float y = elem_to_float(m.fb, bb[l]);
+      v[l] = fl_flush(__fmul_rn(x, y), m.sub_out_flush);
+    } else {
+      v[l] = 0.0f;
+    }
+  }
+#pragma unroll
+  for (int w = 1; w < K; w *= 2) {
+#pragma unroll
+    for (int l = 0; l + w < K; l += 2 * w)
+      if (l + w < nt) v[l] = fl_flush(__fadd_rn(v[l], v[l + w]), m.sub_out_flush);
+  }
+  uint32_t cb = cbits;
+  if (m.c_sub_keep == 0u && (cb & 0x7F800000u) == 0u) cb &= 0x80000000u;
+  float c = __uint_as_float(cb);
+  float r = nt > 0 ? fl_flush(__fadd_rn(c, v[0]), m.sub_out_flush) : fl_flush(c, m.sub_out_flush);
+  if (r != r) return m.nan_bits;
+  return __float_as_uint(r);
+}
+
+// ---------------------------------------------------------------------------
+// one block FMA of nt <= K products under any floating-point architecture.
+// a[l], b[l] are raw element bit patterns.
+// ---------------------------------------------------------------------------
+template <int K, class UT, class AT>
+__device__ __forceinline__ uint32_t block_fma_bits(const DevModel &m, const uint32_t (&ab)[K],
+                                                   const uint32_t (&bb)[K], int nt, uint32_t cbits,
+                                                   bool any_special) {
+  if (m.arch == MCEMU_ARCH_PAIRWISE) return arch_pairwise<K>(m, ab, bb, nt, cbits);
+  Term<UT> p[K];
+#pragma unroll
+  for (int l = 0; l < K; l++) p[l] = make_term<UT>(m, ab[l], bb[l]);
+  uint32_t cS, cneg;
+  int32_t cE;
+  decode_c(m, cbits, cS, cE, cneg);
+  uint32_t spec = 0;
+  if (any_special) {
+#pragma unroll
+    for (int l = 0; l < K; l++)
+      if (l < nt) spec |= product_special(m, ab[l], bb[l]);
+    spec |= c_special(cbits);
+  }
+  if (m.prod_ovf) {
+#pragma unroll
+    for (int l = 0; l < K; l++)
+      if (l < nt) spec |= product_overflow<UT>(m, p[l]);
+  }
+  if (spec) return resolve_special(m, spec);
+  switch (m.arch) {
+    case MCEMU_ARCH_GA_EARLY: return arch_ga_early<K, UT, AT>(m, p, nt, cS, cE, cneg);
+    case MCEMU_ARCH_GA_LATE: return arch_ga_late<K, UT, AT>(m, p, nt, cS, cE, cneg);
+    case MCEMU_ARCH_ODD_EVEN: return arch_odd_even<K, UT, AT>(m, p, nt, cS, cE, cneg);
+    default: return arch_exact<K, UT>(m, p, nt, cS, cE, cneg);
+  }
+}
+
+// integer formats: sum of K byte products plus the int32 c, wrapped or clamped
+template <int K>
+__device__ __forceinline__ uint32_t block_int(const DevModel &m, const uint32_t (&ab)[K],
+                                              const uint32_t (&bb)[K], int nt, uint32_t cbits) {
+  int32_t s = 0;
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if (l < nt) {
+      int32_t x = m.fa.is_signed ? (int32_t)(int8_t)(uint8_t)ab[l] : (int32_t)(uint8_t)ab[l];
+      int32_t y = m.fb.is_signed ? (int32_t)(int8_t)(uint8_t)bb[l] : (int32_t)(uint8_t)bb[l];
+      s += x * y;
+    }
+  if (m.int_sat) {
+    int64_t t = (int64_t)s + (int64_t)(int32_t)cbits;
+    t = t > INT32_MAX ? INT32_MAX : (t < INT32_MIN ? INT32_MIN : t);
+    return (uint32_t)(int32_t)t;
+  }
+  return (uint32_t)s + cbits;
+}
+
+}  // namespace mcemu
+
+namespace mcemu {
+// Any model, any block size up to 32: one out-of-line copy per translation unit
+// for the general (non-specialised) kernels.  64-bit significand arithmetic.
+static __device__ __noinline__ uint32_t block_eval_generic(const DevModel &m, const uint32_t *ea,
+                                                           const uint32_t *eb, int nt, uint32_t cbits) {
+  uint32_t a[32], b[32];
+  bool anys = (cbits & 0x7F800000u) == 0x7F800000u;
+#pragma unroll
+  for (int l = 0; l < 32; l++) {
+    a[l] = l < nt ? ea[l] : 0u;
+    b[l] = l < nt ? eb[l] : 0u;
+    if (l < nt) anys = anys || special_word(m.fa, a[l]) || special_word(m.fb, b[l]);
+  }
+  if (m.fa.is_int) return block_int<32>(m, a, b, nt, cbits);
+  return block_fma_bits<32, uint64_t, int64_t>(m, a, b, nt, cbits, anys);
+}
+}  // namespace mcemu

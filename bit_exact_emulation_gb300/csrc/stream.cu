@@ -1,0 +1,223 @@
+// stream.cu -- the block-FMA stream: one vector set (a[0..k-1], b[0..k-1], c)
+// per thread, eq. (1) of "Accurate Models of AMD Matrix Cores" under the model.
+//
+// The data are read once, so the kernel is a grid-stride stream of 8-, 16- or
+// 32-byte vector loads with the evict-first cache hint; the work per vector is
+// integer ALU (decode, significand products, max, shifts, one normalisation).
+#include <cuda_runtime.h>
+
+#include "core.cuh"
+
+namespace mcemu {
+
+// container sizes: CT 1/2/4 = bytes per element (4 = XF32-style, <= 11-bit
+// significands), CT 5 = full binary32 inputs (48-bit significand products)
+template <int CT> struct CtBytes { static constexpr int v = CT == 5 ? 4 : CT; };
+
+template <int NB>
+__device__ __forceinline__ void load_words(const uint8_t *p, uint32_t (&w)[(NB + 3) / 4]) {
+  if constexpr (NB == 1) {
+    w[0] = __ldcs(p);
+  } else if constexpr (NB == 2) {
+    w[0] = __ldcs(reinterpret_cast<const unsigned short *>(p));
+  } else if constexpr (NB == 4) {
+    w[0] = __ldcs(reinterpret_cast<const unsigned int *>(p));
+  } else if constexpr (NB == 8) {
+    uint2 v = __ldcs(reinterpret_cast<const uint2 *>(p));
+    w[0] = v.x; w[1] = v.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < NB / 16; i++) {
+      uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p) + i);
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+  }
+}
+
+template <int ESZ, int K, int NW>
+__device__ __forceinline__ void split_elems(const uint32_t (&w)[NW], uint32_t (&e)[K], int nt) {
+#pragma unroll
+  for (int l = 0; l < K; l++) {
+    uint32_t x = 0;
+    if (l < nt) {
+      if constexpr (ESZ == 1) x = (w[l / 4] >> (8 * (l % 4))) & 0xFFu;
+      else if constexpr (ESZ == 2) x = (w[l / 2] >> (16 * (l % 2))) & 0xFFFFu;
+      else x = w[l];
+    }
+    e[l] = x;
+  }
+}
+
+// Floating-point models.  KM is the compile-time maximum of the model's block
+// size k (k <= KM, extra slots are predicated off); vectors are k elements apart.
+template <int ARCH, int CT, int KM, bool WIDE>
+__global__ void __launch_bounds__(256) block_fma_kernel(const DevModel m, size_t n,
+                                                        const uint8_t *__restrict__ a,
+                                                        const uint8_t *__restrict__ b,
+                                                        const uint32_t *__restrict__ c,
+                                                        uint32_t *__restrict__ d) {
+  constexpr int ESZ = CtBytes<CT>::v;
+  using UT = typename std::conditional<(WIDE || CT == 5), uint64_t, uint32_t>::type;
+  using AT = typename std::conditional<(WIDE || CT == 5), int64_t, int32_t>::type;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
+    // the dispatcher selects this kernel only for k == KM: one vector load per operand
+    constexpr int NB = KM * ESZ;
+    uint32_t wa[(NB + 3) / 4], wb[(NB + 3) / 4];
+    load_words<NB>(a + v * NB, wa);
+    load_words<NB>(b + v * NB, wb);
+    uint32_t sw = 0;
+#pragma unroll
+    for (int i = 0; i < (NB + 3) / 4; i++) sw |= special_word(m.fa, wa[i]) | special_word(m.fb, wb[i]);
+    bool anys = sw != 0;
+    uint32_t ea[KM], eb[KM];
+    split_elems<ESZ, KM>(wa, ea, KM);
+    split_elems<ESZ, KM>(wb, eb, KM);
+    uint32_t cb = __ldcs(c + v);
+    anys = anys || (cb & 0x7F800000u) == 0x7F800000u;
+    DevModel mm = m;
+    mm.arch = ARCH;                     // lets the compiler drop the other architectures
+    uint32_t r = block_fma_bits<KM, UT, AT>(mm, ea, eb, KM, cb, anys);
+    __stcs(d + v, r);
+  }
+}
+
+// Integer formats (INT8/UINT8): exact int32 dot product plus c.
+template <int KM>
+__global__ void __launch_bounds__(256) block_int_kernel(const DevModel m, size_t n,
+                                                        const uint8_t *__restrict__ a,
+                                                        const uint8_t *__restrict__ b,
+                                                        const uint32_t *__restrict__ c,
+                                                        uint32_t *__restrict__ d) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const bool ss = m.fa.is_signed && m.fb.is_signed, uu = !m.fa.is_signed && !m.fb.is_signed;
+  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
+    uint32_t wa[KM / 4], wb[KM / 4];
+    load_words<KM>(a + v * KM, wa);
+    load_words<KM>(b + v * KM, wb);
+    int32_t s = 0;       // exact: |sum| <= 32 * 255 * 255
+    if (ss) {
+#pragma unroll
+      for (int i = 0; i < KM / 4; i++) s = __dp4a((int)wa[i], (int)wb[i], s);
+    } else if (uu) {
+#pragma unroll
+      for (int i = 0; i < KM / 4; i++) s = (int32_t)__dp4a(wa[i], wb[i], (unsigned)s);
+    } else {
+      uint32_t ea[KM], eb[KM];
+      split_elems<1, KM>(wa, ea, KM);
+      split_elems<1, KM>(wb, eb, KM);
+      s = (int32_t)block_int<KM>(m, ea, eb, KM, 0u);
+    }
+    uint32_t cb = __ldcs(c + v);
+    uint32_t r;
+    if (m.int_sat) {
+      int64_t t = (int64_t)s + (int64_t)(int32_t)cb;
+      t = t > INT32_MAX ? INT32_MAX : (t < INT32_MIN ? INT32_MIN : t);
+      r = (uint32_t)(int32_t)t;
+    } else {
+      r = (uint32_t)s + cb;
+    }
+    __stcs(d + v, r);
+  }
+}
+
+// Any model: element loads, the out-of-line evaluator (the fallback for
+// combinations without a specialised kernel).
+__global__ void __launch_bounds__(256) block_generic_kernel(const DevModel m, size_t n, int eb,
+                                                            const uint8_t *__restrict__ a,
+                                                            const uint8_t *__restrict__ b,
+                                                            const uint32_t *__restrict__ c,
+                                                            uint32_t *__restrict__ d) {
+  const int k = m.k;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
+    uint32_t ea[32], ebv[32];
+    for (int l = 0; l < k; l++) {
+      size_t idx = v * k + l;
+      if (eb == 1) { ea[l] = a[idx]; ebv[l] = b[idx]; }
+      else if (eb == 2) { ea[l] = reinterpret_cast<const uint16_t *>(a)[idx]; ebv[l] = reinterpret_cast<const uint16_t *>(b)[idx]; }
+      else { ea[l] = reinterpret_cast<const uint32_t *>(a)[idx]; ebv[l] = reinterpret_cast<const uint32_t *>(b)[idx]; }
+    }
+    d[v] = block_eval_generic(m, ea, ebv, k, c[v]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dispatch: specialised kernels for the block sizes and formats of the
+// workloads and the hardware presets; everything else takes the generic kernel
+// ---------------------------------------------------------------------------
+static int grid_for(size_t n, const void *kernel) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+  if (per_sm < 1) per_sm = 1;
+  size_t want = (n + 255) / 256;
+  size_t full = (size_t)sms * per_sm;              // one wave of resident blocks
+  if (want > full) want = full;
+  return (int)(want < 1 ? 1 : want);
+}
+
+typedef void (*FpKernel)(const DevModel, size_t, const uint8_t *, const uint8_t *, const uint32_t *, uint32_t *);
+
+struct Special {
+  int arch, ct, km, wide;
+  FpKernel fn;
+};
+
+#define SPEC(A, C, K, W) {A, C, K, W, block_fma_kernel<A, C, K, W>}
+static const Special kSpecial[] = {
+    // GA_EARLY (the randomized-workload truncate / RNE models; Table 3 presets)
+    SPEC(MCEMU_ARCH_GA_EARLY, 2, 4, false), SPEC(MCEMU_ARCH_GA_EARLY, 2, 8, false),
+    SPEC(MCEMU_ARCH_GA_EARLY, 2, 16, true), SPEC(MCEMU_ARCH_GA_EARLY, 1, 8, false),
+    SPEC(MCEMU_ARCH_GA_EARLY, 1, 16, false), SPEC(MCEMU_ARCH_GA_EARLY, 1, 32, true),
+    SPEC(MCEMU_ARCH_GA_EARLY, 4, 2, false), SPEC(MCEMU_ARCH_GA_EARLY, 4, 4, false),
+    SPEC(MCEMU_ARCH_GA_EARLY, 4, 8, true),
+    // Algorithm 1 (CDNA 3 fp16/bf16: N_FMA 8; tf19: 4)
+    SPEC(MCEMU_ARCH_GA_LATE, 2, 8, false), SPEC(MCEMU_ARCH_GA_LATE, 2, 4, false),
+    SPEC(MCEMU_ARCH_GA_LATE, 4, 4, false),
+    // Algorithm 2 (CDNA 3 binary8: N_FMA 16)
+    SPEC(MCEMU_ARCH_ODD_EVEN, 1, 16, false), SPEC(MCEMU_ARCH_ODD_EVEN, 1, 8, false),
+    // exact-then-round
+    SPEC(MCEMU_ARCH_EXACT, 2, 4, false), SPEC(MCEMU_ARCH_EXACT, 1, 8, false),
+    SPEC(MCEMU_ARCH_EXACT, 4, 2, false), SPEC(MCEMU_ARCH_EXACT, 2, 8, false),
+    SPEC(MCEMU_ARCH_EXACT, 4, 4, false),
+    // pair-wise (CDNA 2)
+    SPEC(MCEMU_ARCH_PAIRWISE, 2, 4, false), SPEC(MCEMU_ARCH_PAIRWISE, 2, 2, false),
+};
+#undef SPEC
+
+int launch_block_fma(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c,
+                     uint32_t *d, void *stream) {
+  if (n == 0) return MCEMU_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (m.fa.is_int && (m.k == 16 || m.k == 8 || m.k == 32 || m.k == 4)) {
+    auto run = [&](auto kern) {
+      int grid = grid_for(n, (const void *)kern);
+      kern<<<grid, 256, 0, s>>>(m, n, (const uint8_t *)a, (const uint8_t *)b, c, d);
+      return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
+    };
+    if (m.k == 4) return run(block_int_kernel<4>);
+    if (m.k == 8) return run(block_int_kernel<8>);
+    if (m.k == 16) return run(block_int_kernel<16>);
+    return run(block_int_kernel<32>);
+  }
+  if (!m.fa.is_int) {
+    // container class: 1, 2 bytes; 4 = reduced XF32; 5 = full binary32 significands
+    const int ct = (m.mab > 22) ? 5 : (int)(m.fa.sshift + 1) / 8;
+    const bool exact_or_pair = m.arch == MCEMU_ARCH_EXACT || m.arch == MCEMU_ARCH_PAIRWISE;
+    for (const Special &sp : kSpecial) {
+      if (sp.arch != m.arch || sp.ct != ct || sp.km != m.k) continue;
+      if (!exact_or_pair && sp.wide != (m.wide != 0)) continue;
+      int grid = grid_for(n, (const void *)sp.fn);
+      sp.fn<<<grid, 256, 0, s>>>(m, n, (const uint8_t *)a, (const uint8_t *)b, c, d);
+      return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
+    }
+  }
+  const int eb = m.fa.is_int ? 1 : (int)(m.fa.sshift + 1) / 8;
+  int grid = grid_for(n, (const void *)block_generic_kernel);
+  block_generic_kernel<<<grid, 256, 0, s>>>(m, n, eb, (const uint8_t *)a, (const uint8_t *)b, c, d);
+  return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
+}
+
+}  // namespace mcemu

@@ -1,0 +1,214 @@
+"""Emulated GEMMs on the GPU (dense tile GEMM, 2:4 compression and sparse GEMM,
+multi-word GEMM), bit for bit against the oracle through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle.presets import PRESETS, block_models
+from bit_exact_emulation_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_exact_emulation_gb300 import build
+    build.build()
+    from bit_exact_emulation_gb300 import binding
+    return binding
+
+
+def dev(x):
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        x = x.view(np.int16)
+    elif x.dtype == np.uint32:
+        x = x.view(np.int32)
+    return torch.from_numpy(x).cuda()
+
+
+def host_u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def all_entries(M, N):
+    ii, jj = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    return ii.ravel().astype(np.int32), jj.ravel().astype(np.int32)
+
+
+def operands(fmt, M, N, K, seed, enc="ocp", special_rate=0.0):
+    rng = np.random.default_rng(seed)
+    if fmt == "bf16" and special_rate == 0.0:
+        A, Bt, C = W.gen_dense_bf16(M, N, K, seed)
+        return A, Bt, C
+    A = W.independent_bits(rng, fmt, (M, K), enc, special_rate)
+    Bt = W.independent_bits(rng, fmt, (N, K), enc, special_rate)
+    if fmt in ("int8", "uint8"):
+        C = rng.integers(0, 1 << 32, (M, N), dtype=np.uint64).astype(np.uint32)
+    else:
+        C = rng.standard_normal((M, N), dtype=np.float32).view(np.uint32)
+    return A, Bt, C
+
+
+GEMM_CASES = [  # model, tile K (instruction inner size), input format
+    (PRESETS["cdna3_bf16"], 8, "bf16"),                 # 32x32x8 bf16_1k, N_FMA 8
+    (PRESETS["cdna3_fp16"], 16, "fp16"),                # 16x16x16 f16
+    (PRESETS["cdna3_xf32"], 8, "xf32"),                 # 16x16x8 xf32, N_FMA 4
+    (PRESETS["cdna3_fp8"], 32, "e4m3"),                 # 16x16x32 fp8, Algorithm 2
+    (PRESETS["cdna1_bf16"], 8, "bf16"),                 # exact, N_FMA 2
+    (PRESETS["cdna2_fp16"], 16, "fp16"),                # pair-wise
+    (PRESETS["b200_fp16"], 16, "fp16"),
+    (block_models("bf16", 4)["ga_trunc"], 8, "bf16"),
+    (block_models("bf16", 4)["ga_rne"], 8, "bf16"),
+    (block_models("bf16", 4)["ieee_exact"], 8, "bf16"),
+    (dict(fmt_a="int8", fmt_b="int8", arch="exact", n_fma=16), 16, "int8"),
+]
+
+
+@pytest.mark.parametrize("case", range(len(GEMM_CASES)))
+@pytest.mark.parametrize("shape", [(37, 29, 100), (16, 16, 8), (1, 1, 3)])
+def test_tile_gemm_full(L, case, shape):
+    spec, kt, fmt = GEMM_CASES[case]
+    M, N, K = shape
+    enc = spec.get("fp8_enc", "ocp")
+    A, Bt, C = operands(fmt, M, N, K, seed=case, enc=enc, special_rate=0.01 if fmt != "bf16" else 0.0)
+    m = L.Model(spec)
+    D = host_u32(L.tile_gemm(m, L.tile(0, 16, 16, kt, 4), dev(A), dev(Bt), dev(C)))
+    ii, jj = all_entries(M, N)
+    want = oracle.gemm_entries(spec, K, kt, A, Bt, C, ii, jj).reshape(M, N)
+    bad = np.argwhere(D != want)
+    assert len(bad) == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
+
+
+def test_tile_gemm_specials_and_zero_k(L):
+    spec = PRESETS["cdna3_bf16"]
+    A, Bt, C = operands("bf16", 20, 20, 64, seed=5, special_rate=0.03)
+    m = L.Model(spec)
+    D = host_u32(L.tile_gemm(m, L.tile(0, 32, 32, 8, 4), dev(A), dev(Bt), dev(C)))
+    ii, jj = all_entries(20, 20)
+    assert np.array_equal(D.ravel(), oracle.gemm_entries(spec, 64, 8, A, Bt, C, ii, jj))
+    # K = 0: D = C
+    A0 = torch.empty((20, 0), dtype=torch.int16, device="cuda")
+    D0 = host_u32(L.tile_gemm(m, L.tile(0, 32, 32, 8, 4), A0, A0, dev(C)))
+    assert np.array_equal(D0, C)
+
+
+def test_dense_bf16_2048_sampled(L):
+    """The dense BF16 GEMM workload: M = N = K = 2048, 32x32x8 bf16 tile semantics."""
+    M = N = K = 2048
+    A, Bt, C = W.gen_dense_bf16(M, N, K, seed=3)
+    rng = np.random.default_rng(11)
+    ii = rng.integers(0, M, 192).astype(np.int32)
+    jj = rng.integers(0, N, 192).astype(np.int32)
+    for spec in (PRESETS["cdna3_bf16"], block_models("bf16", 4)["ga_trunc"]):
+        m = L.Model(spec)
+        D = host_u32(L.tile_gemm(m, L.tile(0, 32, 32, 8, 4), dev(A), dev(Bt), dev(C)))
+        want = oracle.gemm_entries(spec, K, 8, A, Bt, C, ii, jj)
+        assert np.array_equal(D[ii, jj], want)
+
+
+# ---------------------------------------------------------------------------
+# 2:4 sparsity
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt,enc", [("e4m3", "ocp"), ("e4m3", "fnuz"), ("fp16", "ocp"), ("bf16", "ocp"),
+                                     ("int8", "ocp")])
+def test_sparse24_compress_matches_oracle(L, fmt, enc):
+    rng = np.random.default_rng(1)
+    M, K = 97, 128
+    A = W.independent_bits(rng, fmt, (M, K), enc, 0.01)
+    # zero out two thirds of the entries so that most groups have <= 2 nonzeros
+    A[rng.random((M, K)) < 0.6] = 0
+    Ac, meta, viol = L.sparse24_compress(fmt, dev(A), enc)
+    rAc, rmeta, rviol = oracle.sparse24_compress(fmt, A, enc)
+    assert np.array_equal(Ac.cpu().numpy().view(A.dtype), rAc)
+    assert np.array_equal(meta.cpu().numpy(), rmeta)
+    assert int(viol.item()) == rviol and rviol > 0
+
+
+def test_sparse24_expand_inverts_compress(L):
+    A, Bt, C = W.gen_sparse_e4m3(64, 8, 256, seed=4)
+    Ac, meta, viol = L.sparse24_compress("e4m3", dev(A))
+    assert int(viol.item()) == 0
+    E = L.sparse24_expand("e4m3", Ac, meta, 256)
+    assert np.array_equal(E.cpu().numpy(), A)
+
+
+SPARSE_CASES = [
+    dict(fmt_a="e4m3", fmt_b="e4m3", arch="ga_early", n_fma=8, align_frac=26, out_round="rtz"),
+    dict(fmt_a="e4m3", fmt_b="e4m3", arch="ga_early", n_fma=8, align_frac=26, out_round="rne"),
+    dict(fmt_a="e4m3", fmt_b="e4m3", arch="exact", n_fma=8),
+    dict(PRESETS["cdna3_fp8"], fp8_enc="ocp", n_fma=8),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SPARSE_CASES)))
+def test_sparse24_gemm_full(L, case):
+    spec = SPARSE_CASES[case]
+    M, N, K = 45, 33, 160
+    A, Bt, C = W.gen_sparse_e4m3(M, N, K, seed=case, c_zero=False)
+    Ac, meta, _ = oracle.sparse24_compress("e4m3", A)
+    m = L.Model(spec)
+    D = host_u32(L.sparse24_gemm(m, L.tile(1, 16, 16, 32, 8), dev(Ac), dev(meta), dev(Bt), dev(C)))
+    ii, jj = all_entries(M, N)
+    want = oracle.sparse24_entries(spec, K, 32, Ac, meta, Bt, C, ii, jj).reshape(M, N)
+    assert np.array_equal(D, want), f"{int((D != want).sum())} mismatches"
+
+
+def test_sparse_e4m3_4096_sampled(L):
+    """The 2:4 E4M3 workload at full size: A 4096x4096 compressed to 4096x2048, 16x16x32 tiles."""
+    M = N = K = 4096
+    A, Bt, C = W.gen_sparse_e4m3(M, N, K, seed=4)
+    dA = dev(A)
+    Ac, meta, viol = L.sparse24_compress("e4m3", dA)
+    assert int(viol.item()) == 0
+    spec = SPARSE_CASES[0]
+    m = L.Model(spec)
+    D = host_u32(L.sparse24_gemm(m, L.tile(1, 16, 16, 32, 8), Ac, meta, dev(Bt), dev(C)))
+    rng = np.random.default_rng(12)
+    ii = rng.integers(0, M, 128).astype(np.int32)
+    jj = rng.integers(0, N, 128).astype(np.int32)
+    hAc, hmeta = Ac.cpu().numpy(), meta.cpu().numpy()
+    want = oracle.sparse24_entries(spec, K, 32, hAc, hmeta, Bt, C, ii, jj)
+    assert np.array_equal(D[ii, jj], want)
+
+
+# ---------------------------------------------------------------------------
+# multi-word GEMM
+# ---------------------------------------------------------------------------
+def test_multiword_split_matches_oracle(L):
+    A, _ = W.gen_multiword_fp64(64, 1, 96, seed=5)
+    w = L.multiword_split(torch.from_numpy(A).cuda(), 3).cpu().numpy().view(np.uint16)
+    assert np.array_equal(w, oracle.split_bf16(A, 3))
+
+
+@pytest.mark.parametrize("truncated", [False, True])
+@pytest.mark.parametrize("word_model", ["cdna3_bf16", "ga_trunc"])
+def test_multiword_gemm_full(L, truncated, word_model):
+    spec = PRESETS["cdna3_bf16"] if word_model == "cdna3_bf16" else block_models("bf16", 8)["ga_trunc"]
+    M, N, K = 19, 23, 72
+    A, Bt = W.gen_multiword_fp64(M, N, K, seed=6)
+    m = L.Model(spec)
+    D = L.multiword_gemm(m, L.tile(0, 32, 32, 8, 4), 3, truncated, torch.from_numpy(A).cuda(),
+                         torch.from_numpy(Bt).cuda()).cpu().numpy()
+    ii, jj = all_entries(M, N)
+    want = oracle.multiword_entries(spec, 8, 3, truncated, A, Bt, ii, jj).reshape(M, N)
+    assert np.array_equal(D.view(np.uint64), want.view(np.uint64))
+
+
+def test_multiword_error_report(L):
+    M, N, K = 64, 48, 256
+    A, Bt = W.gen_multiword_fp64(M, N, K, seed=7)
+    m = L.Model(PRESETS["cdna3_bf16"])
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(Bt).cuda()
+    errs = []
+    for truncated in (False, True):
+        D = L.multiword_gemm(m, L.tile(0, 32, 32, 8, 4), 3, truncated, dA, dB)
+        R = dA @ dB.T
+        e2, r2 = L.fro_error(D, R).cpu().numpy()
+        errs.append(np.sqrt(e2 / r2))
+        ref = np.sqrt(((D.cpu().numpy() - R.cpu().numpy()) ** 2).sum() / (R.cpu().numpy() ** 2).sum())
+        assert abs(errs[-1] - ref) <= 1e-12 * max(ref, 1e-300)
+    assert errs[0] < 1e-5 and errs[1] < 1e-5

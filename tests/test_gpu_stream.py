@@ -1,0 +1,217 @@
+"""Block-FMA stream on the GPU, bit for bit against the oracle (and the paper's
+printed outputs), through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle.presets import PRESETS, block_models
+from bit_exact_emulation_gb300 import workloads as W
+from _golden import encode_row, fp32_expect_bits, load_vectors
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_exact_emulation_gb300 import build
+    build.build()
+    from bit_exact_emulation_gb300 import binding
+    return binding
+
+
+def dev(x):
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        x = x.view(np.int16)
+    elif x.dtype == np.uint32:
+        x = x.view(np.int32)
+    return torch.from_numpy(x).cuda()
+
+
+def gpu_block(L, spec, a, b, c):
+    m = L.Model(spec)
+    d = L.block_fma(m, dev(a), dev(b), dev(c))
+    return d.cpu().numpy().view(np.uint32)
+
+
+def gpu_chain(L, spec, kt, a, b, c):
+    """1 x 1 x K GEMM: the chained block FMAs of one output."""
+    m = L.Model(spec)
+    t = L.tile(0, 16, 16, kt, 4)
+    D = L.tile_gemm(m, t, dev(a), dev(b), dev(np.asarray(c, np.uint32).reshape(1, 1)))
+    return int(D.cpu().numpy().view(np.uint32)[0, 0])
+
+
+def mismatches(got, want, a=None, b=None, c=None, limit=8):
+    bad = np.nonzero(got != want)[0]
+    msg = [f"{len(bad)} of {len(want)} differ"]
+    for v in bad[:limit]:
+        extra = f" a={a[v]} b={b[v]} c={c[v]:#010x}" if a is not None else ""
+        msg.append(f"  [{v}] gpu {got[v]:#010x} oracle {want[v]:#010x}{extra}")
+    return "\n".join(msg)
+
+
+# ---------------------------------------------------------------------------
+# the paper's feature vectors
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("fixture", ["cdna3_algorithm1.txt", "cdna1_exact.txt", "cdna3_algorithm2.txt",
+                                     "cdna2_pairwise.txt"])
+def test_paper_vectors_gpu(L, fixture):
+    bad = []
+    for row in load_vectors(fixture):
+        spec = PRESETS[row["preset"]]
+        a, b, c = encode_row(row, spec.get("fp8_enc", "ocp"))
+        dt = W.ELEM_DTYPE[row["fmt"]]
+        want = fp32_expect_bits(row["expect"], spec["nan_bits"])
+        n = len(a)
+        kt = row["kt"] if row["kt"] else spec["n_fma"]
+        got_chain = gpu_chain(L, spec, kt, np.array([a], dt), np.array([b], dt), c)
+        if got_chain != want:
+            bad.append(f"{row['id']} (chain): gpu {got_chain:#010x} printed {want:#010x}")
+        if row["kt"] == 0:
+            # stream path: pad the vector with zero products (0 * 1) to the block size
+            k = spec["n_fma"]
+            one = W.encode_exact(1, row["fmt"], spec.get("fp8_enc", "ocp"))
+            ap = np.array([a + [0] * (k - n)], dt)
+            bp = np.array([b + [one] * (k - n)], dt)
+            got = int(gpu_block(L, spec, ap, bp, np.array([c], np.uint32))[0])
+            ref = int(oracle.block_fma(spec, ap, bp, np.array([c], np.uint32))[0])
+            if got != ref:
+                bad.append(f"{row['id']} (stream): gpu {got:#010x} oracle {ref:#010x}")
+    assert not bad, "\n".join(bad[:20])
+
+
+# ---------------------------------------------------------------------------
+# randomized vector sets (the validation workloads)
+# ---------------------------------------------------------------------------
+def test_fp16_cancellation_set_all_models(L):
+    """65,536 FP16 K=4 vector sets (half of them with clustered exponents), FP32 c."""
+    a, b, c = W.gen_fp16_cancellation(65536, 4, seed=1)
+    for name, spec in block_models("fp16", 4).items():
+        got = gpu_block(L, spec, a, b, c)
+        want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+        assert np.array_equal(got, want), name + "\n" + mismatches(got, want, a, b, c)
+
+
+FORMAT_SETS = [("fp16", 4, "ocp"), ("bf16", 4, "ocp"), ("xf32", 2, "ocp"), ("e4m3", 8, "ocp"),
+               ("e5m2", 8, "ocp"), ("int8", 16, "ocp")]
+
+
+@pytest.mark.parametrize("fmt,k,enc", FORMAT_SETS)
+def test_independent_bits_with_specials(L, fmt, k, enc):
+    """Independent bit sampling with 1% each of zeros, subnormals, Inf and NaN."""
+    a, b, c = W.gen_block_fma_set(fmt, 40000, k, seed=2 + k, enc=enc)
+    for name, spec in block_models(fmt, k).items():
+        spec = dict(spec, fp8_enc=enc)
+        got = gpu_block(L, spec, a, b, c)
+        want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+        assert np.array_equal(got, want), f"{fmt} {name}\n" + mismatches(got, want, a, b, c)
+
+
+@pytest.mark.parametrize("fmt,k,enc", FORMAT_SETS)
+def test_full_size_sampled(L, fmt, k, enc):
+    """10^7 vector sets per format on the GPU; a seeded sample is recomputed by the oracle."""
+    n = 10_000_000
+    a, b, c = W.gen_block_fma_set(fmt, n, k, seed=2 + k, enc=enc)
+    idx = np.random.default_rng(7).choice(n, 3000, replace=False)
+    for name, spec in block_models(fmt, k).items():
+        got = gpu_block(L, spec, a, b, c)[idx]
+        want = oracle.block_fma_parallel(spec, a[idx], b[idx], c[idx], threads=8)
+        assert np.array_equal(got, want), f"{fmt} {name}\n" + mismatches(got, want)
+
+
+# exponent-mantissa sampling (Algorithm 3, seed 0) at the exponent limits of Sec. 5.1
+CDNA3_SAMPLING = [
+    ("cdna3_fp16", "fp16", (-14, 15), (-126, 127)), ("cdna3_fp16", "fp16", (-24, -14), (-149, -126)),
+    ("cdna3_bf16", "bf16", (-126, 63), (-126, 127)), ("cdna3_bf16", "bf16", (-133, -126), (-149, -126)),
+    ("cdna3_xf32", "xf32", (-126, 63), (-126, 127)), ("cdna3_xf32", "xf32", (-136, -126), (-149, -126)),
+    ("cdna3_fp8", "e4m3", (-7, 7), (-126, 127)), ("cdna3_fp8", "e4m3", (-10, -7), (-149, -126)),
+    ("cdna3_bf8", "e5m2", (-15, 15), (-126, 127)), ("cdna3_bf8", "e5m2", (-17, -15), (-149, -126)),
+]
+
+
+@pytest.mark.parametrize("preset,fmt,eab,ec", CDNA3_SAMPLING)
+def test_cdna3_exponent_mantissa_sampling(L, preset, fmt, eab, ec):
+    spec = PRESETS[preset]
+    a, b, c = W.gen_exp_mantissa(fmt, 60000, spec["n_fma"], eab, ec, seed=0,
+                                 enc=spec.get("fp8_enc", "ocp"))
+    got = gpu_block(L, spec, a, b, c)
+    want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+    assert np.array_equal(got, want), preset + "\n" + mismatches(got, want, a, b, c)
+
+
+GENERIC_CASES = [
+    ("exact", "fp16", 1), ("exact", "bf16", 3), ("ga_early", "bf16", 5), ("ga_late", "fp16", 12),
+    ("odd_even", "e4m3", 32), ("ga_early", "e5m2", 32), ("pairwise", "bf16", 8), ("exact", "xf32", 16),
+    ("ga_late", "bf16", 16), ("exact", "fp32", 1), ("exact", "fp32", 3), ("ga_early", "fp32", 2),
+    ("pairwise", "fp32", 1), ("ga_early", "fp16", 16), ("exact", "e4m3", 32),
+]
+
+
+@pytest.mark.parametrize("arch,fmt,k", GENERIC_CASES)
+@pytest.mark.parametrize("variant", ["plain", "flush_rd_fnuz"])
+def test_every_architecture_any_block_size(L, arch, fmt, k, variant):
+    base = dict(fmt_a=fmt, fmt_b=fmt, arch=arch, n_fma=k, align_frac=24, c_zero_exp=-126,
+                prod_overflow=True, nan_bits=0xFFC00000, pair_group=k)
+    if arch == "ga_early":
+        base.update(align_frac=25, c_zero_exp=None, emin_lim=-133, out_round="rtz")
+    if variant == "flush_rd_fnuz":
+        base.update(sub_in_flush=True, sub_out_flush=True, fp8_enc="fnuz", xf32_round="rne")
+        if arch in ("ga_early",):
+            base.update(align_round="rd")
+    enc = base.get("fp8_enc", "ocp")
+    a, b, c = W.gen_block_fma_set(fmt, 8000, k, seed=31 + k, enc=enc, special_rate=0.02)
+    got = gpu_block(L, base, a, b, c)
+    want = oracle.block_fma_parallel(base, a, b, c, threads=8)
+    assert np.array_equal(got, want), f"{arch} {fmt} k={k} {variant}\n" + mismatches(got, want, a, b, c)
+
+
+def test_mixed_fp8_operands(L):
+    spec = dict(PRESETS["cdna3_fp8"], fmt_b="e5m2")
+    a = W.gen_exp_mantissa("e4m3", 20000, 16, (-7, 7), (-126, 127), seed=0, enc="fnuz")[0]
+    b, _, c = W.gen_exp_mantissa("e5m2", 20000, 16, (-15, 15), (-126, 127), seed=1, enc="fnuz")
+    got = gpu_block(L, spec, a, b, c)
+    want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+    assert np.array_equal(got, want), mismatches(got, want)
+
+
+@pytest.mark.parametrize("sat", [False, True])
+@pytest.mark.parametrize("fa,fb", [("int8", "int8"), ("uint8", "uint8"), ("int8", "uint8")])
+def test_integer_formats(L, fa, fb, sat):
+    rng = np.random.default_rng(3)
+    n = 50000
+    a = rng.integers(0, 256, (n, 16), dtype=np.uint64).astype(np.uint8)
+    b = rng.integers(0, 256, (n, 16), dtype=np.uint64).astype(np.uint8)
+    c = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+    c[:100] = 0x7FFFFFF0
+    c[100:200] = 0x80000010
+    spec = dict(fmt_a=fa, fmt_b=fb, arch="exact", n_fma=16, int_saturate=sat)
+    got = gpu_block(L, spec, a, b, c)
+    want = oracle.block_fma(spec, a, b, c)
+    assert np.array_equal(got, want), mismatches(got, want)
+
+
+def test_empty_single_and_ragged(L):
+    spec = block_models("bf16", 4)["ga_trunc"]
+    m = L.Model(spec)
+    e = torch.empty(0, dtype=torch.int16, device="cuda")
+    d = L.block_fma(m, e, e, torch.empty(0, dtype=torch.int32, device="cuda"))
+    assert d.numel() == 0
+    for n in (1, 2, 255, 257, 100003):
+        a, b, c = W.gen_block_fma_set("bf16", n, 4, seed=n)
+        got = gpu_block(L, spec, a, b, c)
+        assert np.array_equal(got, oracle.block_fma(spec, a, b, c))
+
+
+def test_misaligned_pointer_is_rejected(L):
+    spec = block_models("fp16", 4)["ga_rne"]
+    m = L.Model(spec)
+    buf = torch.zeros(4 * 64 + 8, dtype=torch.int16, device="cuda")
+    a = buf[1:1 + 4 * 64]                        # 2-byte offset: not 8-byte aligned
+    c = torch.zeros(64, dtype=torch.int32, device="cuda")
+    with pytest.raises(L.McemuError) as e:
+        L.block_fma(m, a, a, c)
+    assert e.value.status == 4
