@@ -1,0 +1,403 @@
+"""Benchmark: bit-exact emulated block-FMAs/s on GB300 (and emulated-GEMM GFLOP/s).
+
+A step is one pass of the block-FMA stream over the randomized-validation workload:
+10^7 vector sets for each of FP16 K=4, BF16 K=4, XF32 K=2, FP8 E4M3 K=8, FP8 E5M2
+K=8 (OCP) under three models (truncate, round-to-nearest-even, exact-then-round) and
+INT8 K=16 (int32 accumulate); inputs by independent bit sampling with 1% each of
+zeros, subnormals, Inf and NaN.  16 launches, 1.6e8 block FMAs per step and GPU.
+The dense BF16 (2048^3), 2:4 sparse E4M3 (4096^3) and multi-word FP64 (4096^3)
+GEMMs are timed in the same run and reported under "gemm".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  Under torchrun each rank processes its own vector
+sets (weak scaling, no collective on the data path).
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_exact_emulation_gb300 import workloads as W  # noqa: E402
+
+N_VEC = 10_000_000
+FORMATS = [("fp16", 4), ("bf16", 4), ("xf32", 2), ("e4m3", 8), ("e5m2", 8), ("int8", 16)]
+MODELS = ("ga_trunc", "ga_rne", "ieee_exact")
+METRIC = "bit-exact emulated block-FMAs/sec (10^7 vector sets x 6 formats x 3 models)"
+VEC_BYTES = {f: k * (1 if f in ("e4m3", "e5m2", "int8") else (2 if f in ("fp16", "bf16") else 4))
+             for f, k in FORMATS}
+
+
+def workload_models(fmt, k):
+    """(name, model description) of the stream models for one format (library presets)."""
+    from bit_exact_emulation_gb300 import binding as L
+    if fmt == "int8":
+        return [("int", L.preset_desc("ieee_exact", "int8", k))]
+    return [(name, L.preset_desc(name, fmt, k)) for name in MODELS]
+
+
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sms, mx, reasons = [], None, set()
+        for line in out.strip().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sms.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sms)) if sms else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU baseline (the oracle, as it stands) -- also the bench's parity sample
+# ---------------------------------------------------------------------------
+def cpu_baseline(data, outputs, per_combo, threads):
+    import oracle
+    from oracle.presets import block_models
+    total, t_total, mismatches = 0, 0.0, 0
+    for fmt, k in FORMATS:
+        a, b, c = data[fmt]
+        idx = np.random.default_rng(99).choice(a.shape[0], per_combo, replace=False)
+        idx.sort()
+        for name, spec in block_models(fmt, k).items():
+            t0 = time.perf_counter()
+            want = oracle.block_fma_parallel(spec, a[idx], b[idx], c[idx], threads)
+            t_total += time.perf_counter() - t0
+            total += per_combo
+            got = outputs.get((fmt, name))
+            if got is not None:
+                mismatches += int((got[idx] != want).sum())
+    return total, t_total, mismatches
+
+
+def run_reference(args, rank):
+    """The reference arm: the oracle on the host cores, a bounded sample per step."""
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    per_combo = 30000
+    data = {fmt: W.gen_block_fma_set(fmt, 2 * per_combo, k, seed=2 + k) for fmt, k in FORMATS}
+    for _ in range(args.warmup):
+        cpu_baseline(data, {}, per_combo // 10, threads)
+    n = 0
+    t = 0.0
+    for _ in range(args.steps):
+        cnt, dt, _ = cpu_baseline(data, {}, per_combo, threads)
+        n += cnt
+        t += dt
+    value = n / t
+    sample = f"{per_combo} vector sets per (format, model) pair per step, 16 pairs, CPU oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "block-FMA/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int (exact big-integer)",
+            "data": "synthetic", "config": {"workload": "randomized block-FMA vector sets (bounded sample)"},
+            "cpu_baseline": {"value": value, "unit": "block-FMA/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "block-FMA/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_exact_emulation_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kernel_key):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_source_hash()
+    for line in open(path):
+        p = [x.strip() for x in line.strip().strip("|").split("|")]
+        if len(p) >= 3 and p[0] == kernel_key and p[2] == cur:
+            try:
+                return float(p[1])
+            except ValueError:
+                return None
+    return None
+
+
+def gemm_section(L, torch, dev, steps):
+    """Time the three emulated-GEMM workloads; returns their summary dict."""
+    out = {}
+    s = torch.cuda.current_stream()
+
+    def timed(fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps / 1000.0
+
+    # dense BF16 2048^3, 32x32x8 bf16 tile semantics
+    M = N = K = 2048
+    A, Bt, C = W.gen_dense_bf16(M, N, K, seed=3)
+    dA, dB, dC = dev(A), dev(Bt), dev(C)
+    t = L.tile(0, 32, 32, 8, 4)
+    dense = {}
+    for name, desc in (("cdna3_bf16", L.preset_desc("cdna3_bf16")), ("ga_trunc_k4", L.preset_desc("ga_trunc", "bf16", 4)),
+                       ("ga_rne_k4", L.preset_desc("ga_rne", "bf16", 4)), ("ieee_exact_k4", L.preset_desc("ieee_exact", "bf16", 4))):
+        m = L.Model(desc)
+        D = torch.empty((M, N), dtype=torch.int32, device="cuda")
+        sec = timed(lambda: L.tile_gemm(m, t, dA, dB, dC, D), steps)
+        dense[name] = {"ms": sec * 1e3, "gflops": 2.0 * M * N * K / sec / 1e9}
+    out["dense_bf16_2048"] = dense
+    del dA, dB, dC
+    # 2:4 sparse E4M3 4096^3, 16x16x32 tile semantics
+    M = N = K = 4096
+    A, Bt, C = W.gen_sparse_e4m3(M, N, K, seed=4)
+    dA, dB, dC = dev(A), dev(Bt), dev(C)
+    Ac, meta, viol = L.sparse24_compress("e4m3", dA)
+    tcomp = timed(lambda: L.sparse24_compress("e4m3", dA), steps)
+    ts = L.tile(1, 16, 16, 32, 8)
+    sparse = {"compress_ms": tcomp * 1e3, "compress_gbs": (M * K * 1.5 + M * K / 2 + M * K / 4) / tcomp / 1e9,
+              "violations": int(viol.item())}
+    for name in ("ga_trunc", "ga_rne"):
+        m = L.Model(L.preset_desc(name, "e4m3", 8))
+        D = torch.empty((M, N), dtype=torch.int32, device="cuda")
+        sec = timed(lambda: L.sparse24_gemm(m, ts, Ac, meta, dB, dC, D), steps)
+        sparse[name] = {"ms": sec * 1e3, "gflops_effective": 2.0 * M * N * (K // 2) / sec / 1e9,
+                        "gflops_dense_equivalent": 2.0 * M * N * K / sec / 1e9}
+    out["sparse24_e4m3_4096"] = sparse
+    del dA, dB, dC, Ac, meta
+    # multi-word FP64 4096^3: 3 BF16 words, 9 and 6 word products, CDNA3 BF16 word model
+    A, Bt = W.gen_multiword_fp64(M, N, K, seed=5)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(Bt).cuda()
+    m = L.Model(L.preset_desc("cdna3_bf16"))
+    ws = torch.empty(L.multiword_workspace(3, M, N, K), dtype=torch.uint8, device="cuda")
+    D = torch.empty((M, N), dtype=torch.float64, device="cuda")
+    R = dA @ dB.T
+    mw = {}
+    for label, trunc, npairs in (("9_products", False, 9), ("6_products", True, 6)):
+        sec = timed(lambda: L.multiword_gemm(m, t, 3, trunc, dA, dB, D, ws), max(1, steps // 2))
+        e2, r2 = L.fro_error(D, R).cpu().numpy()
+        mw[label] = {"ms": sec * 1e3, "gflops_emulated": npairs * 2.0 * M * N * K / sec / 1e9,
+                     "rel_fro_error": float(np.sqrt(e2 / r2))}
+    out["multiword_fp64_4096"] = mw
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-gemm", action="store_true", help="skip the GEMM section (stream numbers only)")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    from bit_exact_emulation_gb300 import build
+    build.build()
+    from bit_exact_emulation_gb300 import binding as L
+
+    def dev(x):
+        x = np.ascontiguousarray(x)
+        if x.dtype == np.uint16:
+            x = x.view(np.int16)
+        elif x.dtype == np.uint32:
+            x = x.view(np.int32)
+        return torch.from_numpy(x).cuda()
+
+    # inputs: this rank's own vector sets (weak scaling)
+    data, gpu, launches = {}, {}, []
+    for fmt, k in FORMATS:
+        a, b, c = W.gen_block_fma_set(fmt, N_VEC, k, seed=2 + k + 1000 * rank)
+        data[fmt] = (a, b, c)
+        gpu[fmt] = (dev(a), dev(b), dev(c))
+        for name, desc in workload_models(fmt, k):
+            m = L.Model(desc)
+            d = torch.empty(N_VEC, dtype=torch.int32, device="cuda")
+            launches.append((fmt, name, m, d))
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in launches]
+
+    def step(record=False):
+        for li, (fmt, name, m, d) in enumerate(launches):
+            a, b, c = gpu[fmt]
+            if record:
+                evs[li][0].record(stream)
+            L.block_fma(m, a, b, c, d)
+            if record:
+                evs[li][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    per_launch = np.zeros(len(launches))
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+        t1.record(stream)
+        t1.synchronize()
+        for li in range(len(launches)):
+            per_launch[li] += evs[li][0].elapsed_time(evs[li][1])
+    torch.cuda.synchronize()
+    elapsed_ms = t0.elapsed_time(t1)
+    clk = clocks.stop()
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+        dist.barrier()
+    ms_per_step = elapsed_ms / args.steps
+    fmas_per_step = N_VEC * len(launches)
+    value = fmas_per_step * world / (ms_per_step / 1e3)
+
+    # outputs of the last step for the parity sample
+    outputs = {(fmt, name): d.cpu().numpy().view(np.uint32) for fmt, name, m, d in launches}
+
+    # roofline of the dominant kernel: algorithmic bytes = n * (2 * vector bytes + 8) per launch
+    per_launch /= args.steps
+    dom = int(np.argmax(per_launch))
+    dfmt, dname = launches[dom][0], launches[dom][1]
+    algo_bytes = N_VEC * (2 * VEC_BYTES[dfmt] + 8)
+    achieved = algo_bytes / (per_launch[dom] / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+    roofline = {"bound": "hbm", "kernel": f"block_fma {dfmt} {dname}", "achieved": achieved, "peak": peak,
+                "peak_source": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": read_traffic(f"block_fma {dfmt} {dname}"),
+                "algorithmic_bytes_per_launch": algo_bytes,
+                "per_kernel_gbs": {f"{f} {n}": N_VEC * (2 * VEC_BYTES[f] + 8) / (t / 1e3) / 1e9
+                                   for (f, n, _, _), t in zip(launches, per_launch)}}
+
+    # end to end through the host-buffer entry point (pinned host memory, copies timed)
+    e2e = None
+    if rank == 0:
+        pinned = {}
+        for fmt, k in FORMATS:
+            a, b, c = data[fmt]
+            pinned[fmt] = tuple(torch.from_numpy(np.ascontiguousarray(x).view(
+                {np.uint16: np.int16, np.uint32: np.int32}.get(x.dtype.type, x.dtype))).pin_memory() for x in (a, b, c))
+        outs = [torch.empty(N_VEC, dtype=torch.int32).pin_memory() for _ in launches]
+        ws = torch.empty(max(L.block_fma_host_workspace(m) for _, _, m, _ in launches), dtype=torch.uint8,
+                         device="cuda")
+
+        def e2e_step():
+            for li, (fmt, name, m, d) in enumerate(launches):
+                a, b, c = pinned[fmt]
+                L.block_fma_host(m, a, b, c, outs[li], ws)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        te = time.perf_counter()
+        e2e_steps = max(1, min(args.steps, 2))
+        for _ in range(e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        te = (time.perf_counter() - te) / e2e_steps
+        h2d = sum(N_VEC * (2 * VEC_BYTES[f] + 4) for f, _, _, _ in launches)
+        e2e = {"value": fmas_per_step / te, "unit": "block-FMA/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": N_VEC * 4 * len(launches), "ms_per_step": te * 1e3,
+               "api": "mcemu_block_fma_host"}
+        for li, (fmt, name, m, d) in enumerate(launches):
+            if not np.array_equal(outs[li].numpy().view(np.uint32), outputs[(fmt, name)]):
+                e2e["mismatch"] = f"{fmt} {name}"
+
+    gemm = None
+    if rank == 0 and not args.no_gemm:
+        gemm = gemm_section(L, torch, dev, max(1, min(args.steps, 3)))
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    per_combo = 100_000
+    n_cpu, t_cpu, mism = cpu_baseline(data, outputs, per_combo, threads)
+    cpu = {"value": n_cpu / t_cpu, "unit": "block-FMA/s", "cores": threads, "kind": "oracle",
+           "sample": f"{per_combo} seeded vector sets of each (format, model) pair of the step, "
+                     f"{n_cpu} block FMAs; the same sample checks the GPU outputs"}
+    line = {"metric": METRIC, "value": value, "unit": "block-FMA/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int32/int64 integer significand arithmetic", "data": "synthetic",
+            "config": {"workload": "randomized block-FMA vector sets: 10^7 each of FP16 K=4, BF16 K=4, XF32 K=2, "
+                                   "E4M3 K=8, E5M2 K=8 (OCP) x {truncate, RNE, exact} + INT8 K=16",
+                       "vector_sets_per_step_per_gpu": fmas_per_step, "launches_per_step": len(launches),
+                       "l2": "inputs larger than L2 (200-400 MB read per launch)",
+                       "parity_sample_mismatches": mism, "parity_sample": n_cpu},
+            "gpu_launches": len(launches) * args.steps, "clocks": clk, "roofline": roofline,
+            "cpu_baseline": cpu, "e2e": e2e, "gemm": gemm}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
