@@ -240,10 +240,12 @@ def gemm_section(L, torch, dev, steps):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-gemm", action="store_true", help="skip the GEMM section (stream numbers only)")
+    ap.add_argument("--vectors", type=int, default=N_VEC,
+                    help="vector sets per (format, model) launch; smaller values are for profiling runs only")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -269,15 +271,16 @@ def main():
             x = x.view(np.int32)
         return torch.from_numpy(x).cuda()
 
+    n_vec = args.vectors
     # inputs: this rank's own vector sets (weak scaling)
     data, gpu, launches = {}, {}, []
     for fmt, k in FORMATS:
-        a, b, c = W.gen_block_fma_set(fmt, N_VEC, k, seed=2 + k + 1000 * rank)
+        a, b, c = W.gen_block_fma_set(fmt, n_vec, k, seed=2 + k + 1000 * rank)
         data[fmt] = (a, b, c)
         gpu[fmt] = (dev(a), dev(b), dev(c))
         for name, desc in workload_models(fmt, k):
             m = L.Model(desc)
-            d = torch.empty(N_VEC, dtype=torch.int32, device="cuda")
+            d = torch.empty(n_vec, dtype=torch.int32, device="cuda")
             launches.append((fmt, name, m, d))
     stream = torch.cuda.current_stream()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in launches]
@@ -319,7 +322,7 @@ def main():
         elapsed_ms = float(tt.item())
         dist.barrier()
     ms_per_step = elapsed_ms / args.steps
-    fmas_per_step = N_VEC * len(launches)
+    fmas_per_step = n_vec * len(launches)
     value = fmas_per_step * world / (ms_per_step / 1e3)
 
     # outputs of the last step for the parity sample
@@ -329,14 +332,14 @@ def main():
     per_launch /= args.steps
     dom = int(np.argmax(per_launch))
     dfmt, dname = launches[dom][0], launches[dom][1]
-    algo_bytes = N_VEC * (2 * VEC_BYTES[dfmt] + 8)
+    algo_bytes = n_vec * (2 * VEC_BYTES[dfmt] + 8)
     achieved = algo_bytes / (per_launch[dom] / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
     roofline = {"bound": "hbm", "kernel": f"block_fma {dfmt} {dname}", "achieved": achieved, "peak": peak,
                 "peak_source": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": read_traffic(f"block_fma {dfmt} {dname}"),
                 "algorithmic_bytes_per_launch": algo_bytes,
-                "per_kernel_gbs": {f"{f} {n}": N_VEC * (2 * VEC_BYTES[f] + 8) / (t / 1e3) / 1e9
+                "per_kernel_gbs": {f"{f} {n}": n_vec * (2 * VEC_BYTES[f] + 8) / (t / 1e3) / 1e9
                                    for (f, n, _, _), t in zip(launches, per_launch)}}
 
     # end to end through the host-buffer entry point (pinned host memory, copies timed)
@@ -347,7 +350,7 @@ def main():
             a, b, c = data[fmt]
             pinned[fmt] = tuple(torch.from_numpy(np.ascontiguousarray(x).view(
                 {np.uint16: np.int16, np.uint32: np.int32}.get(x.dtype.type, x.dtype))).pin_memory() for x in (a, b, c))
-        outs = [torch.empty(N_VEC, dtype=torch.int32).pin_memory() for _ in launches]
+        outs = [torch.empty(n_vec, dtype=torch.int32).pin_memory() for _ in launches]
         ws = torch.empty(max(L.block_fma_host_workspace(m) for _, _, m, _ in launches), dtype=torch.uint8,
                          device="cuda")
 
@@ -364,9 +367,9 @@ def main():
             e2e_step()
         torch.cuda.synchronize()
         te = (time.perf_counter() - te) / e2e_steps
-        h2d = sum(N_VEC * (2 * VEC_BYTES[f] + 4) for f, _, _, _ in launches)
+        h2d = sum(n_vec * (2 * VEC_BYTES[f] + 4) for f, _, _, _ in launches)
         e2e = {"value": fmas_per_step / te, "unit": "block-FMA/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": N_VEC * 4 * len(launches), "ms_per_step": te * 1e3,
+               "d2h_bytes_per_step": n_vec * 4 * len(launches), "ms_per_step": te * 1e3,
                "api": "mcemu_block_fma_host"}
         for li, (fmt, name, m, d) in enumerate(launches):
             if not np.array_equal(outs[li].numpy().view(np.uint32), outputs[(fmt, name)]):
@@ -381,7 +384,7 @@ def main():
     if rank != 0:
         return
     threads = os.cpu_count() or 1
-    per_combo = 100_000
+    per_combo = min(100_000, n_vec // 2)
     n_cpu, t_cpu, mism = cpu_baseline(data, outputs, per_combo, threads)
     cpu = {"value": n_cpu / t_cpu, "unit": "block-FMA/s", "cores": threads, "kind": "oracle",
            "sample": f"{per_combo} seeded vector sets of each (format, model) pair of the step, "
@@ -389,7 +392,7 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": "block-FMA/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int32/int64 integer significand arithmetic", "data": "synthetic",
-            "config": {"workload": "randomized block-FMA vector sets: 10^7 each of FP16 K=4, BF16 K=4, XF32 K=2, "
+            "config": {"workload": f"randomized block-FMA vector sets: {n_vec:.0e} each of FP16 K=4, BF16 K=4, XF32 K=2, "
                                    "E4M3 K=8, E5M2 K=8 (OCP) x {truncate, RNE, exact} + INT8 K=16",
                        "vector_sets_per_step_per_gpu": fmas_per_step, "launches_per_step": len(launches),
                        "l2": "inputs larger than L2 (200-400 MB read per launch)",
