@@ -48,43 +48,9 @@ __device__ __forceinline__ void split_elems(const uint32_t (&w)[NW], uint32_t (&
   }
 }
 
-// Floating-point models.  KM is the compile-time maximum of the model's block
-// size k (k <= KM, extra slots are predicated off); vectors are k elements apart.
-template <int ARCH, int CT, int KM, bool WIDE>
-__global__ void __launch_bounds__(256) block_fma_kernel(const DevModel m, size_t n,
-                                                        const uint8_t *__restrict__ a,
-                                                        const uint8_t *__restrict__ b,
-                                                        const uint32_t *__restrict__ c,
-                                                        uint32_t *__restrict__ d) {
-  constexpr int ESZ = CtBytes<CT>::v;
-  using UT = typename std::conditional<(WIDE || CT == 5), uint64_t, uint32_t>::type;
-  using AT = typename std::conditional<(WIDE || CT == 5), int64_t, int32_t>::type;
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
-    // the dispatcher selects this kernel only for k == KM: one vector load per operand
-    constexpr int NB = KM * ESZ;
-    uint32_t wa[(NB + 3) / 4], wb[(NB + 3) / 4];
-    load_words<NB>(a + v * NB, wa);
-    load_words<NB>(b + v * NB, wb);
-    uint32_t sw = 0;
-#pragma unroll
-    for (int i = 0; i < (NB + 3) / 4; i++) sw |= special_word(m.fa, wa[i]) | special_word(m.fb, wb[i]);
-    bool anys = sw != 0;
-    uint32_t ea[KM], eb[KM];
-    split_elems<ESZ, KM>(wa, ea, KM);
-    split_elems<ESZ, KM>(wb, eb, KM);
-    uint32_t cb = __ldcs(c + v);
-    anys = anys || (cb & 0x7F800000u) == 0x7F800000u;
-    DevModel mm = m;
-    mm.arch = ARCH;                     // lets the compiler drop the other architectures
-    uint32_t r = block_fma_bits<KM, UT, AT>(mm, ea, eb, KM, cb, anys);
-    __stcs(d + v, r);
-  }
-}
-
 // Integer formats (INT8/UINT8): exact int32 dot product plus c.
 template <int KM>
-__global__ void __launch_bounds__(256) block_int_kernel(const DevModel m, size_t n,
+__global__ void __launch_bounds__(256) block_int_kernel(const __grid_constant__ DevModel m, size_t n,
                                                         const uint8_t *__restrict__ a,
                                                         const uint8_t *__restrict__ b,
                                                         const uint32_t *__restrict__ c,
@@ -121,9 +87,37 @@ __global__ void __launch_bounds__(256) block_int_kernel(const DevModel m, size_t
   }
 }
 
+// Specialised kernel: architecture, format and block size fixed at compile time.
+template <int ARCH, int ID, int KM, bool WIDE>
+__global__ void __launch_bounds__(256) fast_kernel(const __grid_constant__ DevModel m, size_t n,
+                                                   const uint8_t *__restrict__ a, const uint8_t *__restrict__ b,
+                                                   const uint32_t *__restrict__ c, uint32_t *__restrict__ d) {
+  constexpr int NB = KM * Fmt<ID>::BYTES;
+  constexpr int NW = (NB + 3) / 4;
+  using UT = typename std::conditional<(WIDE || ID == F_FP32), uint64_t, uint32_t>::type;
+  using AT = typename std::conditional<(WIDE || ID == F_FP32), int64_t, int32_t>::type;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
+    uint32_t wa[NW], wb[NW];
+    load_words<NB>(a + v * NB, wa);
+    load_words<NB>(b + v * NB, wb);
+    const uint32_t cb = __ldcs(c + v);
+    uint32_t sw = (cb & 0x7F800000u) == 0x7F800000u;
+#pragma unroll
+    for (int i = 0; i < NW; i++) sw |= fspecial_word<ID>(wa[i]) | fspecial_word<ID>(wb[i]);
+    uint32_t ea[KM], eb[KM];
+#pragma unroll
+    for (int l = 0; l < KM; l++) {
+      ea[l] = felem<ID>(wa, l);
+      eb[l] = felem<ID>(wb, l);
+    }
+    __stcs(d + v, block_fma_fast<ARCH, ID, KM, UT, AT>(m, ea, eb, cb, sw != 0));
+  }
+}
+
 // Any model: element loads, the out-of-line evaluator (the fallback for
 // combinations without a specialised kernel).
-__global__ void __launch_bounds__(256) block_generic_kernel(const DevModel m, size_t n, int eb,
+__global__ void __launch_bounds__(256) block_generic_kernel(const __grid_constant__ DevModel m, size_t n, int eb,
                                                             const uint8_t *__restrict__ a,
                                                             const uint8_t *__restrict__ b,
                                                             const uint32_t *__restrict__ c,
@@ -161,31 +155,44 @@ static int grid_for(size_t n, const void *kernel) {
 typedef void (*FpKernel)(const DevModel, size_t, const uint8_t *, const uint8_t *, const uint32_t *, uint32_t *);
 
 struct Special {
-  int arch, ct, km, wide;
+  int arch, id, km, wide;
   FpKernel fn;
 };
 
-#define SPEC(A, C, K, W) {A, C, K, W, block_fma_kernel<A, C, K, W>}
+#define SPEC(A, F, K, W) {A, F, K, W, fast_kernel<A, F, K, W>}
 static const Special kSpecial[] = {
-    // GA_EARLY (the randomized-workload truncate / RNE models; Table 3 presets)
-    SPEC(MCEMU_ARCH_GA_EARLY, 2, 4, false), SPEC(MCEMU_ARCH_GA_EARLY, 2, 8, false),
-    SPEC(MCEMU_ARCH_GA_EARLY, 2, 16, true), SPEC(MCEMU_ARCH_GA_EARLY, 1, 8, false),
-    SPEC(MCEMU_ARCH_GA_EARLY, 1, 16, false), SPEC(MCEMU_ARCH_GA_EARLY, 1, 32, true),
-    SPEC(MCEMU_ARCH_GA_EARLY, 4, 2, false), SPEC(MCEMU_ARCH_GA_EARLY, 4, 4, false),
-    SPEC(MCEMU_ARCH_GA_EARLY, 4, 8, true),
-    // Algorithm 1 (CDNA 3 fp16/bf16: N_FMA 8; tf19: 4)
-    SPEC(MCEMU_ARCH_GA_LATE, 2, 8, false), SPEC(MCEMU_ARCH_GA_LATE, 2, 4, false),
-    SPEC(MCEMU_ARCH_GA_LATE, 4, 4, false),
-    // Algorithm 2 (CDNA 3 binary8: N_FMA 16)
-    SPEC(MCEMU_ARCH_ODD_EVEN, 1, 16, false), SPEC(MCEMU_ARCH_ODD_EVEN, 1, 8, false),
-    // exact-then-round
-    SPEC(MCEMU_ARCH_EXACT, 2, 4, false), SPEC(MCEMU_ARCH_EXACT, 1, 8, false),
-    SPEC(MCEMU_ARCH_EXACT, 4, 2, false), SPEC(MCEMU_ARCH_EXACT, 2, 8, false),
-    SPEC(MCEMU_ARCH_EXACT, 4, 4, false),
-    // pair-wise (CDNA 2)
-    SPEC(MCEMU_ARCH_PAIRWISE, 2, 4, false), SPEC(MCEMU_ARCH_PAIRWISE, 2, 2, false),
+    // early-c global alignment: the randomized-workload truncate / RNE models
+    SPEC(MCEMU_ARCH_GA_EARLY, F_FP16, 4, false), SPEC(MCEMU_ARCH_GA_EARLY, F_BF16, 4, false),
+    SPEC(MCEMU_ARCH_GA_EARLY, F_XF32T, 2, false), SPEC(MCEMU_ARCH_GA_EARLY, F_E4M3, 8, false),
+    SPEC(MCEMU_ARCH_GA_EARLY, F_E5M2, 8, false),
+    // exact-then-round on the same vector sets
+    SPEC(MCEMU_ARCH_EXACT, F_FP16, 4, false), SPEC(MCEMU_ARCH_EXACT, F_BF16, 4, false),
+    SPEC(MCEMU_ARCH_EXACT, F_XF32T, 2, false), SPEC(MCEMU_ARCH_EXACT, F_E4M3, 8, false),
+    SPEC(MCEMU_ARCH_EXACT, F_E5M2, 8, false),
+    // CDNA 3: Algorithm 1 (fp16/bf16 N_FMA 8, tf19 4), Algorithm 2 (binary8 FNUZ, 16)
+    SPEC(MCEMU_ARCH_GA_LATE, F_FP16, 8, false), SPEC(MCEMU_ARCH_GA_LATE, F_BF16, 8, false),
+    SPEC(MCEMU_ARCH_GA_LATE, F_XF32T, 4, false), SPEC(MCEMU_ARCH_ODD_EVEN, F_E4M3Z, 16, false),
+    SPEC(MCEMU_ARCH_ODD_EVEN, F_E5M2Z, 16, false),
+    // Table 3 NVIDIA-like presets
+    SPEC(MCEMU_ARCH_GA_EARLY, F_FP16, 16, true), SPEC(MCEMU_ARCH_GA_EARLY, F_FP16, 8, false),
+    SPEC(MCEMU_ARCH_GA_EARLY, F_BF16, 8, false), SPEC(MCEMU_ARCH_GA_EARLY, F_XF32T, 4, false),
 };
 #undef SPEC
+
+// compile-time format of a model whose operands share one format, else -1
+static int fmt_id(const DevModel &m) {
+  const FmtDev &a = m.fa, &b = m.fb;
+  if (a.is_int || a.mbits != b.mbits || a.bias != b.bias || a.xf32 != b.xf32 || a.sw_fnuz != b.sw_fnuz ||
+      a.emask != b.emask)
+    return -1;
+  if (a.xf32) return a.xf32 == 2 ? F_XF32R : F_XF32T;
+  if (a.mbits == 23) return F_FP32;
+  if (a.mbits == 10) return F_FP16;
+  if (a.mbits == 7) return F_BF16;
+  if (a.mbits == 3) return a.sw_fnuz ? F_E4M3Z : F_E4M3;
+  if (a.mbits == 2) return a.sw_fnuz ? F_E5M2Z : F_E5M2;
+  return -1;
+}
 
 int launch_block_fma(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c,
                      uint32_t *d, void *stream) {
@@ -202,13 +209,12 @@ int launch_block_fma(const DevModel &m, size_t n, const void *a, const void *b, 
     if (m.k == 16) return run(block_int_kernel<16>);
     return run(block_int_kernel<32>);
   }
-  if (!m.fa.is_int) {
-    // container class: 1, 2 bytes; 4 = reduced XF32; 5 = full binary32 significands
-    const int ct = (m.mab > 22) ? 5 : (int)(m.fa.sshift + 1) / 8;
-    const bool exact_or_pair = m.arch == MCEMU_ARCH_EXACT || m.arch == MCEMU_ARCH_PAIRWISE;
+  const int id = fmt_id(m);
+  // the specialised kernels assume kept subnormals (the fp32 special-value shortcut)
+  if (id >= 0 && m.arch != MCEMU_ARCH_PAIRWISE && m.fa.sub_keep != 0u && m.c_sub_keep != 0u) {
     for (const Special &sp : kSpecial) {
-      if (sp.arch != m.arch || sp.ct != ct || sp.km != m.k) continue;
-      if (!exact_or_pair && sp.wide != (m.wide != 0)) continue;
+      if (sp.arch != m.arch || sp.id != id || sp.km != m.k) continue;
+      if (m.arch != MCEMU_ARCH_EXACT && sp.wide != (m.wide != 0)) continue;
       int grid = grid_for(n, (const void *)sp.fn);
       sp.fn<<<grid, 256, 0, s>>>(m, n, (const uint8_t *)a, (const uint8_t *)b, c, d);
       return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
