@@ -171,6 +171,29 @@ __device__ __forceinline__ uint32_t round_pack32(uint32_t M, int32_t lsb, uint32
   return bits | (neg << 31);
 }
 
+// Hardware rounding of an integer significand: value = S * 2^k.  The int->fp32
+// conversion rounds S to 24 bits exactly as the model's RNE or RTZ does, and
+// scaling by powers of two is exact while the result stays normal; an overflow
+// gives Inf under RN and the largest finite under RZ, as the model does.  A
+// subnormal result would be rounded twice, so those (and zero) return false
+// and the caller takes the integer path.
+__device__ __forceinline__ bool hw_scale(float x, int32_t k, int rne, uint32_t &bits) {
+  const int32_t k1 = min(max(k, -96), 96);           // |x| in [1, 2^63): x*2^k1 stays normal
+  const int32_t k2 = min(k - k1, 127);                // beyond 127 the result overflows anyway
+  if (k2 < -126) return false;
+  const float s1 = __uint_as_float((uint32_t)(k1 + 127) << 23);
+  const float s2 = __uint_as_float((uint32_t)(k2 + 127) << 23);
+  const float y = rne ? __fmul_rn(__fmul_rn(x, s1), s2) : __fmul_rz(__fmul_rz(x, s1), s2);
+  bits = __float_as_uint(y);
+  return (bits & 0x7F800000u) != 0u;
+}
+__device__ __forceinline__ bool hw_round32(int32_t S, int32_t k, int rne, uint32_t &bits) {
+  return hw_scale(rne ? __int2float_rn(S) : __int2float_rz(S), k, rne, bits);
+}
+__device__ __forceinline__ bool hw_round64(int64_t S, int32_t k, int rne, uint32_t &bits) {
+  return hw_scale(rne ? __ll2float_rn(S) : __ll2float_rz(S), k, rne, bits);
+}
+
 // ---------------------------------------------------------------------------
 // terms of eq. (1)
 // ---------------------------------------------------------------------------
@@ -240,6 +263,12 @@ __device__ __forceinline__ AT align_term(UT Ushift, uint32_t neg, int32_t sh, in
 
 template <class AT>
 __device__ __forceinline__ uint32_t pack_sum(AT S, int32_t lsb, const DevModel &m) {
+  if (!m.sub_out_flush) {
+    uint32_t bits;
+    const bool ok = (sizeof(AT) == 4) ? hw_round32((int32_t)S, lsb, m.rne, bits)
+                                      : hw_round64((int64_t)S, lsb, m.rne, bits);
+    if (ok) return bits;
+  }
   uint32_t neg = S < 0 ? 1u : 0u;
   if (sizeof(AT) == 4) {
     uint32_t M = neg ? (uint32_t)(-(int32_t)S) : (uint32_t)S;
@@ -294,6 +323,10 @@ __device__ __forceinline__ uint32_t late_c_merge(const DevModel &m, AT Sp, bool 
     }
     int64_t Sacc = (int64_t)Sp + sc;        // line 8
     if (Sacc == 0) return zero_result<K, UT>(p, nt, cS, cneg);
+    if (!m.sub_out_flush) {
+      uint32_t bits;
+      if (hw_round64(Sacc, emax - m.F, m.rne, bits)) return bits;       // line 15
+    }
     uint32_t neg = Sacc < 0 ? 1u : 0u;
     uint64_t M = neg ? (uint64_t)(-Sacc) : (uint64_t)Sacc;
     return round_pack(M, emax - m.F, neg, false, m.rne, m.sub_out_flush);   // line 15
@@ -319,6 +352,10 @@ __device__ __forceinline__ uint32_t late_c_merge(const DevModel &m, AT Sp, bool 
   if (r > 0) {
     M = neg ? ((M + ((1ull << r) - 1ull)) >> r) : (M >> r);   // floor of the signed value
     lsb += r;
+  }
+  if (!m.sub_out_flush) {
+    uint32_t bits;
+    if (hw_round64(neg ? -(int64_t)M : (int64_t)M, lsb, m.rne, bits)) return bits;   // line 15
   }
   return round_pack(M, lsb, neg, false, m.rne, m.sub_out_flush);   // line 15
 }
@@ -389,6 +426,13 @@ __device__ __forceinline__ uint32_t round_pack128(i128 W, int32_t L, bool sticky
   int32_t s = p > 61 ? p - 61 : 0;
   uint64_t M = (uint64_t)(Mag >> s);
   bool st = sticky || (s > 0 && (Mag & (((u128)1 << s) - 1)) != 0);
+  if (!m.sub_out_flush && (p - s) >= 26) {
+    // bit 0 of M lies at least two places below the rounding point, so it can carry
+    // the sticky bit into the hardware conversion
+    const uint64_t Ms = M | (st ? 1ull : 0ull);
+    uint32_t bits;
+    if (hw_round64(neg ? -(int64_t)Ms : (int64_t)Ms, L + s, m.rne, bits)) return bits;
+  }
   return round_pack(M, L + s, neg, st, m.rne, m.sub_out_flush);
 }
 

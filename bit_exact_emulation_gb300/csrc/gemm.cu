@@ -129,6 +129,7 @@ int launch_tile_gemm(const DevModel &m, int kt, int M, int N, int K, const void 
                      int64_t ldd, void *stream) {
   cudaStream_t s = (cudaStream_t)stream;
   if (kt > 1024) return MCEMU_ERR_UNSUPPORTED;
+  if (gemm_fast_ok(m) && kt <= 64) return launch_tile_gemm_fast(m, kt, M, N, K, A, lda, Bt, ldb, C, ldc, D, ldd, stream);
   const size_t shm = (size_t)2 * kT * chunk_len(kt) * 4;
   dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT), block(kT, kT);
   const uint8_t *a = (const uint8_t *)A, *b = (const uint8_t *)Bt;
