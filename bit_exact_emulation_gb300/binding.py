@@ -25,6 +25,7 @@ PRESET = {"cdna3_fp16": 0, "cdna3_bf16": 1, "cdna3_xf32": 2, "cdna3_fp8": 3, "cd
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "not 2:4 sparse", 4: "alignment",
           5: "CUDA error", 6: "timeout", 7: "workspace too small"}
 FRO_OUT_DOUBLES = 1026
+MULTIWORD_STATIC_BYTES = 8 << 20      # MCEMU_MULTIWORD_STATIC_BYTES
 
 
 class McemuError(RuntimeError):
@@ -76,6 +77,8 @@ SYMBOLS = {
     "mcemu_multiword_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 5
                              + [ctypes.c_void_p, ctypes.c_int64] * 3
                              + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "mcemu_multiword_gemm_static": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 5
+                                    + [ctypes.c_void_p, ctypes.c_int64] * 3 + [ctypes.c_void_p]),
     "mcemu_fro_error": (ctypes.c_int, [ctypes.c_int] * 2 + [ctypes.c_void_p, ctypes.c_int64] * 2
                         + [ctypes.c_void_p, ctypes.c_void_p]),
 }
@@ -269,6 +272,19 @@ def multiword_gemm(model: Model, t: TileDesc, n_words: int, truncated: bool, A, 
                                       _p(A), A.stride(0), _p(Bt), Bt.stride(0), _p(D), D.stride(0),
                                       _p(workspace), workspace.numel() * workspace.element_size(),
                                       _stream()), "mcemu_multiword_gemm")
+    return D
+
+
+def multiword_gemm_static(model: Model, t: TileDesc, n_words: int, truncated: bool, A, Bt, D=None):
+    """mcemu_multiword_gemm_static: the multi-word GEMM with the library's fixed scratch."""
+    import torch
+    M, K = A.shape
+    N = Bt.shape[0]
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.float64, device=A.device)
+    _check(lib().mcemu_multiword_gemm_static(model.handle, ctypes.byref(t), n_words, int(bool(truncated)), M, N,
+                                             K, _p(A), A.stride(0), _p(Bt), Bt.stride(0), _p(D), D.stride(0),
+                                             _stream()), "mcemu_multiword_gemm_static")
     return D
 
 

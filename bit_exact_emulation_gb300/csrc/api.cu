@@ -582,6 +582,28 @@ extern "C" int mcemu_multiword_gemm(mcemu_model_t word_model, const mcemu_tile_d
                                N, K, A, lda, Bt, ldb, D, ldd, workspace, ws_bytes, stream);
 }
 
+extern "C" int mcemu_multiword_gemm_static(mcemu_model_t word_model, const mcemu_tile_desc *tile, int n_words,
+                                           int product_set, int M, int N, int K, const double *A, int64_t lda,
+                                           const double *Bt, int64_t ldb, double *D, int64_t ldd, void *stream) {
+  if (!word_model || check_tile(tile) != MCEMU_OK) return MCEMU_ERR_INVALID_ARG;
+  const mcemu_model_desc &wd = word_model->m.desc;
+  if (wd.fmt_a != MCEMU_BF16 || wd.fmt_b != MCEMU_BF16) return MCEMU_ERR_UNSUPPORTED;
+  if (n_words < 1 || n_words > 8) return MCEMU_ERR_INVALID_ARG;
+  if (product_set != MCEMU_WORDS_ALL && product_set != MCEMU_WORDS_TRUNCATED) return MCEMU_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return MCEMU_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return MCEMU_OK;
+  // the words must fit the fixed array (M*K and N*K first, so the size cannot wrap)
+  if ((uint64_t)M * (uint64_t)K > MCEMU_MULTIWORD_STATIC_BYTES ||
+      (uint64_t)N * (uint64_t)K > MCEMU_MULTIWORD_STATIC_BYTES ||
+      mcemu_multiword_workspace(n_words, M, N, K) > MCEMU_MULTIWORD_STATIC_BYTES)
+    return MCEMU_ERR_WORKSPACE;
+  if ((K > 0 && (!A || !Bt)) || !D) return MCEMU_ERR_INVALID_ARG;
+  if (lda < K || ldb < K || ldd < N) return MCEMU_ERR_INVALID_ARG;
+  if (!aligned(A, 8) || !aligned(Bt, 8) || !aligned(D, 8)) return MCEMU_ERR_ALIGNMENT;
+  return launch_multiword_gemm_static(word_model->m.dev, tile->K, n_words, product_set == MCEMU_WORDS_TRUNCATED,
+                                      M, N, K, A, lda, Bt, ldb, D, ldd, stream);
+}
+
 extern "C" int mcemu_fro_error(int M, int N, const double *D, int64_t ldd, const double *R, int64_t ldr,
                                double *out, void *stream) {
   if (M < 0 || N < 0 || !out) return MCEMU_ERR_INVALID_ARG;

@@ -83,6 +83,9 @@ int launch_multiword_split(int n_words, size_t n, const double *x, int64_t ldx, 
 int launch_multiword_gemm(const DevModel &m, int kt, int n_words, int truncated, int M, int N,
                           int K, const double *A, int64_t lda, const double *Bt, int64_t ldb,
                           double *D, int64_t ldd, void *ws, size_t ws_bytes, void *stream);
+int launch_multiword_gemm_static(const DevModel &m, int kt, int n_words, int truncated, int M, int N, int K,
+                                 const double *A, int64_t lda, const double *Bt, int64_t ldb, double *D,
+                                 int64_t ldd, void *stream);
 int launch_fro_error(int M, int N, const double *D, int64_t ldd, const double *R, int64_t ldr,
                      double *out, void *stream);
 

@@ -6,6 +6,9 @@
 // i ascending), so no word-product matrix is ever stored.
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "core.cuh"
 
 namespace mcemu {
@@ -160,6 +163,51 @@ int launch_multiword_gemm(const DevModel &m, int kt, int n_words, int truncated,
     case 3: return run_mw<3>(m, kt, truncated, M, N, K, Aw, Bw, D, ldd, s);
     default: return run_mw<4>(m, kt, truncated, M, N, K, Aw, Bw, D, ldd, s);
   }
+}
+
+// ---------------------------------------------------------------------------
+// The same GEMM for callers that cannot allocate device memory where they call
+// it (a host program that only holds buffers handed to it, a loop whose device
+// memory is budgeted up front): the words of A and B go to a fixed array of this
+// module's device memory instead of caller workspace.  The split kernel writes
+// every word the GEMM kernel reads, so nothing in the array has to start at
+// zero.  One array per device serves every call: calls whose kernels may
+// overlap race on it.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_mw_static_ws[MCEMU_MULTIWORD_STATIC_BYTES];
+
+constexpr int kMaxDevices = 64;
+static std::atomic<void *> g_mw_static_ptr[kMaxDevices];
+static std::mutex g_mw_static_mu;
+
+// device address of the array on the current device; looked up once per device,
+// with that device current (the caller's), then cached
+static void *mw_static_ptr(int &status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { status = MCEMU_ERR_CUDA; return nullptr; }
+  if (dev < 0 || dev >= kMaxDevices) { status = MCEMU_ERR_UNSUPPORTED; return nullptr; }
+  void *p = g_mw_static_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  std::lock_guard<std::mutex> lock(g_mw_static_mu);
+  p = g_mw_static_ptr[dev].load(std::memory_order_relaxed);
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_mw_static_ws) != cudaSuccess || !p) {
+      status = MCEMU_ERR_CUDA;
+      return nullptr;
+    }
+    g_mw_static_ptr[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+int launch_multiword_gemm_static(const DevModel &m, int kt, int n_words, int truncated, int M, int N, int K,
+                                 const double *A, int64_t lda, const double *Bt, int64_t ldb, double *D,
+                                 int64_t ldd, void *stream) {
+  int status = MCEMU_OK;
+  void *ws = mw_static_ptr(status);
+  if (!ws) return status;
+  return launch_multiword_gemm(m, kt, n_words, truncated, M, N, K, A, lda, Bt, ldb, D, ldd, ws,
+                               MCEMU_MULTIWORD_STATIC_BYTES, stream);
 }
 
 // ||D - R||_F^2 and ||R||_F^2 with a fixed reduction order (deterministic)

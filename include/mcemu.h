@@ -242,6 +242,28 @@ int mcemu_multiword_gemm(mcemu_model_t word_model, const mcemu_tile_desc *tile, 
                          const double *Bt, int64_t ldb, double *D, int64_t ldd,
                          void *workspace, size_t ws_bytes, void *stream);
 size_t mcemu_multiword_workspace(int n_words, int M, int N, int K);
+/* ---- multi-word GEMM with no allocation (library addition) ----------------
+ * The paper has no counterpart to this call: it is a convenience of this
+ * library.  It computes exactly what mcemu_multiword_gemm computes (same
+ * kernels, same results bit for bit), but takes no workspace argument: the
+ * BF16 words of A and B are written to a fixed array in the library's own
+ * device memory, MCEMU_MULTIWORD_STATIC_BYTES long.  It is meant for callers
+ * that cannot allocate device memory where they call it: a host program that
+ * only holds device buffers handed to it, or a loop whose device memory was
+ * budgeted up front and must not grow.  The call itself allocates nothing.
+ * Set-up: the first call on each device (the caller's current device) looks up
+ * the array's device address once; make that first call before any stream
+ * capture.  Limit: mcemu_multiword_workspace(n_words, M, N, K) must not exceed
+ * MCEMU_MULTIWORD_STATIC_BYTES, else MCEMU_ERR_WORKSPACE and nothing runs.
+ * Nothing in the array has to start at zero (every word is written before it
+ * is read).  The array is shared by all calls on a device: two calls whose
+ * kernels may overlap (other streams, other host threads) race on it; order
+ * them on one stream.  Other arguments and errors as mcemu_multiword_gemm;
+ * MCEMU_ERR_CUDA when the address look-up fails. */
+#define MCEMU_MULTIWORD_STATIC_BYTES ((size_t)8 << 20)
+int mcemu_multiword_gemm_static(mcemu_model_t word_model, const mcemu_tile_desc *tile, int n_words,
+                                int product_set, int M, int N, int K, const double *A, int64_t lda,
+                                const double *Bt, int64_t ldb, double *D, int64_t ldd, void *stream);
 /* Relative norm-wise error ||D - R||_F / ||R||_F pieces (Sec. 8.1 reports this
  * error): out[0] = sum (D-R)^2, out[1] = sum R^2, summed in a fixed order.
  * out: device, MCEMU_FRO_OUT_DOUBLES doubles; out[2..] is scratch. */
