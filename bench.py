@@ -173,8 +173,8 @@ def read_traffic(kernel_key):
     return None
 
 
-def gemm_section(L, torch, dev, steps):
-    """Time the three emulated-GEMM workloads; returns their summary dict."""
+def gemm_section(L, torch, dev, steps, parts=("dense", "sparse", "multiword")):
+    """Time the emulated-GEMM workloads named in `parts`; returns their summary dict."""
     out = {}
     s = torch.cuda.current_stream()
 
@@ -190,6 +190,16 @@ def gemm_section(L, torch, dev, steps):
         return e0.elapsed_time(e1) / reps / 1000.0
 
     # dense BF16 2048^3, 32x32x8 bf16 tile semantics
+    if "dense" in parts:
+        out["dense_bf16_2048"] = gemm_dense(L, torch, dev, timed, steps)
+    if "sparse" in parts:
+        out["sparse24_e4m3_4096"] = gemm_sparse(L, torch, dev, timed, steps)
+    if "multiword" in parts:
+        out["multiword_fp64_4096"] = gemm_multiword(L, torch, timed, steps)
+    return out
+
+
+def gemm_dense(L, torch, dev, timed, steps):
     M = N = K = 2048
     A, Bt, C = W.gen_dense_bf16(M, N, K, seed=3)
     dA, dB, dC = dev(A), dev(Bt), dev(C)
@@ -201,9 +211,11 @@ def gemm_section(L, torch, dev, steps):
         D = torch.empty((M, N), dtype=torch.int32, device="cuda")
         sec = timed(lambda: L.tile_gemm(m, t, dA, dB, dC, D), steps)
         dense[name] = {"ms": sec * 1e3, "gflops": 2.0 * M * N * K / sec / 1e9}
-    out["dense_bf16_2048"] = dense
-    del dA, dB, dC
-    # 2:4 sparse E4M3 4096^3, 16x16x32 tile semantics
+    return dense
+
+
+def gemm_sparse(L, torch, dev, timed, steps):
+    """2:4 sparse E4M3 4096^3, 16x16x32 tile semantics."""
     M = N = K = 4096
     A, Bt, C = W.gen_sparse_e4m3(M, N, K, seed=4)
     dA, dB, dC = dev(A), dev(Bt), dev(C)
@@ -218,9 +230,13 @@ def gemm_section(L, torch, dev, steps):
         sec = timed(lambda: L.sparse24_gemm(m, ts, Ac, meta, dB, dC, D), steps)
         sparse[name] = {"ms": sec * 1e3, "gflops_effective": 2.0 * M * N * (K // 2) / sec / 1e9,
                         "gflops_dense_equivalent": 2.0 * M * N * K / sec / 1e9}
-    out["sparse24_e4m3_4096"] = sparse
-    del dA, dB, dC, Ac, meta
-    # multi-word FP64 4096^3: 3 BF16 words, 9 and 6 word products, CDNA3 BF16 word model
+    return sparse
+
+
+def gemm_multiword(L, torch, timed, steps):
+    """Multi-word FP64 4096^3: 3 BF16 words, 9 and 6 word products, CDNA3 BF16 word model."""
+    M = N = K = 4096
+    t = L.tile(0, 32, 32, 8, 4)
     A, Bt = W.gen_multiword_fp64(M, N, K, seed=5)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(Bt).cuda()
     m = L.Model(L.preset_desc("cdna3_bf16"))
@@ -233,8 +249,7 @@ def gemm_section(L, torch, dev, steps):
         e2, r2 = L.fro_error(D, R).cpu().numpy()
         mw[label] = {"ms": sec * 1e3, "gflops_emulated": npairs * 2.0 * M * N * K / sec / 1e9,
                      "rel_fro_error": float(np.sqrt(e2 / r2))}
-    out["multiword_fp64_4096"] = mw
-    return out
+    return mw
 
 
 def main():
@@ -244,6 +259,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-gemm", action="store_true", help="skip the GEMM section (stream numbers only)")
+    ap.add_argument("--gemm-parts", default="dense,sparse,multiword",
+                    help="comma list of the GEMM workloads to time (dense, sparse, multiword)")
     ap.add_argument("--vectors", type=int, default=N_VEC,
                     help="vector sets per (format, model) launch; smaller values are for profiling runs only")
     args = ap.parse_args()
@@ -377,7 +394,7 @@ def main():
 
     gemm = None
     if rank == 0 and not args.no_gemm:
-        gemm = gemm_section(L, torch, dev, max(1, min(args.steps, 3)))
+        gemm = gemm_section(L, torch, dev, max(1, min(args.steps, 3)), tuple(args.gemm_parts.split(",")))
 
     if world > 1:
         dist.barrier()

@@ -156,6 +156,8 @@ int launch_sparse24_gemm(const DevModel &m, int kt, int M, int N, int K, const v
                          const uint32_t *C, int64_t ldc, uint32_t *D, int64_t ldd, void *stream) {
   cudaStream_t s = (cudaStream_t)stream;
   if (kt > 1024) return MCEMU_ERR_UNSUPPORTED;
+  if (sparse_fast_ok(m, kt))
+    return launch_sparse24_gemm_fast(m, kt, M, N, K, Ac, ldac, meta, ldm, Bt, ldb, C, ldc, D, ldd, stream);
   const int Kc = K / 2, ktc = kt / 2;
   const size_t shm = (size_t)4 * kT * chunk_len(ktc) * 4;
   dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT), block(kT, kT);

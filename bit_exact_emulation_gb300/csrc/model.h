@@ -69,6 +69,12 @@ bool gemm_fast_ok(const DevModel &m);
 int launch_tile_gemm_fast(const DevModel &m, int kt, int M, int N, int K, const void *A, int64_t lda,
                           const void *Bt, int64_t ldb, const uint32_t *C, int64_t ldc, uint32_t *D, int64_t ldd,
                           void *stream);
+int launch_tile_gemm_fast_acc64(const DevModel &m, int kt, int M, int N, int K, const uint16_t *Aw, int64_t lda,
+                                const uint16_t *Bw, int64_t ldb, double *D, int64_t ldd, int first, void *stream);
+bool sparse_fast_ok(const DevModel &m, int kt);
+int launch_sparse24_gemm_fast(const DevModel &m, int kt, int M, int N, int K, const void *Ac, int64_t ldac,
+                              const uint8_t *meta, int64_t ldm, const void *Bt, int64_t ldb, const uint32_t *C,
+                              int64_t ldc, uint32_t *D, int64_t ldd, void *stream);
 int launch_sparse24_compress(const FmtDev &f, int elem_bytes, int M, int K, const void *A,
                              int64_t lda, void *Ac, int64_t ldac, uint8_t *meta, int64_t ldm,
                              int64_t *viol, void *stream);

@@ -157,6 +157,21 @@ int launch_multiword_gemm(const DevModel &m, int kt, int n_words, int truncated,
     st = launch_multiword_split(n_words, (size_t)N * K, Bt, ldb, N, Bw, (int64_t)N * K, stream);
     if (st != MCEMU_OK) return st;
   }
+  if (gemm_fast_ok(m) && kt <= 64) {
+    // one fast tile GEMM per word pair, each adding its fp32 result into the binary64 D
+    // in the combine order: i + j descending, then i ascending
+    int first = 1;
+    for (int sum = 2 * n_words; sum >= 2; sum--)
+      for (int wi = 1; wi <= n_words; wi++) {
+        const int wj = sum - wi;
+        if (wj < 1 || wj > n_words || (truncated && wi + wj > n_words + 1)) continue;
+        const int st = launch_tile_gemm_fast_acc64(m, kt, M, N, K, Aw + (size_t)(wi - 1) * M * K, K,
+                                                   Bw + (size_t)(wj - 1) * N * K, K, D, ldd, first, stream);
+        if (st != MCEMU_OK) return st;
+        first = 0;
+      }
+    return MCEMU_OK;
+  }
   switch (n_words) {
     case 1: return run_mw<1>(m, kt, truncated, M, N, K, Aw, Bw, D, ldd, s);
     case 2: return run_mw<2>(m, kt, truncated, M, N, K, Aw, Bw, D, ldd, s);

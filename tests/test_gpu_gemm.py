@@ -157,6 +157,31 @@ def test_sparse24_gemm_full(L, case):
     assert np.array_equal(D, want), f"{int((D != want).sum())} mismatches"
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "fp16"])
+@pytest.mark.parametrize("arch", ["ga_early", "ga_late"])
+def test_sparse24_gemm_specials_and_bad_metadata(L, fmt, arch):
+    """Specials in Ac and B, metadata with idx0 >= idx1 and a K that is not a multiple
+    of the instruction: the outputs that leave the fast path take the compressed chain."""
+    rng = np.random.default_rng(21)
+    M, N, K = 70, 67, 200
+    Ac = W.independent_bits(rng, fmt, (M, K // 2), "ocp", 0.001)
+    Bt = W.independent_bits(rng, fmt, (N, K), "ocp", 0.0005)
+    pairs = np.array([0b0100, 0b1000, 0b1100, 0b1001, 0b1101, 0b1110], np.uint8)
+    meta = pairs[rng.integers(0, 6, (M, K // 4))]
+    meta[3, 5] = 0b0101                     # idx0 == idx1
+    meta[10, :] = 0b0011                    # idx0 > idx1 along a whole row
+    C = rng.standard_normal((M, N), dtype=np.float32).view(np.uint32)
+    if arch == "ga_early":
+        spec = dict(fmt_a=fmt, fmt_b=fmt, arch="ga_early", n_fma=8, align_frac=26, out_round="rne")
+    else:
+        spec = dict(PRESETS["cdna3_bf16"], fmt_a=fmt, fmt_b=fmt, n_fma=8)
+    m = L.Model(spec)
+    D = host_u32(L.sparse24_gemm(m, L.tile(1, 16, 16, 32, 8), dev(Ac), dev(meta), dev(Bt), dev(C)))
+    ii, jj = all_entries(M, N)
+    want = oracle.sparse24_entries(spec, K, 32, Ac, meta, Bt, C, ii, jj).reshape(M, N)
+    assert np.array_equal(D, want), f"{int((D != want).sum())} mismatches"
+
+
 def test_sparse_e4m3_4096_sampled(L):
     """The 2:4 E4M3 workload at full size: A 4096x4096 compressed to 4096x2048, 16x16x32 tiles."""
     M = N = K = 4096
@@ -196,6 +221,21 @@ def test_multiword_gemm_full(L, truncated, word_model):
     ii, jj = all_entries(M, N)
     want = oracle.multiword_entries(spec, 8, 3, truncated, A, Bt, ii, jj).reshape(M, N)
     assert np.array_equal(D.view(np.uint64), want.view(np.uint64))
+
+
+@pytest.mark.parametrize("n_words", [1, 2, 4])
+def test_multiword_gemm_word_counts(L, n_words):
+    """Every word count the fast word-product path takes, with a ragged tile edge."""
+    spec = PRESETS["cdna3_bf16"]
+    M, N, K = 66, 65, 40
+    A, Bt = W.gen_multiword_fp64(M, N, K, seed=8 + n_words)
+    m = L.Model(spec)
+    for truncated in (False, True):
+        D = L.multiword_gemm(m, L.tile(0, 32, 32, 8, 4), n_words, truncated, torch.from_numpy(A).cuda(),
+                             torch.from_numpy(Bt).cuda()).cpu().numpy()
+        ii, jj = all_entries(M, N)
+        want = oracle.multiword_entries(spec, 8, n_words, truncated, A, Bt, ii, jj).reshape(M, N)
+        assert np.array_equal(D.view(np.uint64), want.view(np.uint64))
 
 
 def test_multiword_error_report(L):
