@@ -37,6 +37,24 @@ VEC_BYTES = {f: k * (1 if f in ("e4m3", "e5m2", "int8") else (2 if f in ("fp16",
              for f, k in FORMATS}
 
 
+def rank_seed(k, rank):
+    """Seed of one rank's vector sets: every rank streams its own sets (weak scaling)."""
+    return 2 + k + 1000 * rank
+
+
+def max_over_ranks(x, dist, device):
+    """The largest value of x over all ranks (the job takes as long as its slowest rank)."""
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step, world, ms_per_step):
+    """Units all ranks processed per second, over the slowest rank's step time."""
+    return units_per_rank_step * world / (ms_per_step / 1e3)
+
+
 def workload_models(fmt, k):
     """(name, model description) of the stream models for one format (library presets)."""
     from bit_exact_emulation_gb300 import binding as L
@@ -292,7 +310,7 @@ def main():
     # inputs: this rank's own vector sets (weak scaling)
     data, gpu, launches = {}, {}, []
     for fmt, k in FORMATS:
-        a, b, c = W.gen_block_fma_set(fmt, n_vec, k, seed=2 + k + 1000 * rank)
+        a, b, c = W.gen_block_fma_set(fmt, n_vec, k, seed=rank_seed(k, rank))
         data[fmt] = (a, b, c)
         gpu[fmt] = (dev(a), dev(b), dev(c))
         for name, desc in workload_models(fmt, k):
@@ -334,13 +352,11 @@ def main():
     elapsed_ms = t0.elapsed_time(t1)
     clk = clocks.stop()
     if world > 1:
-        tt = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+        elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
         dist.barrier()
     ms_per_step = elapsed_ms / args.steps
     fmas_per_step = n_vec * len(launches)
-    value = fmas_per_step * world / (ms_per_step / 1e3)
+    value = whole_job_rate(fmas_per_step, world, ms_per_step)
 
     # outputs of the last step for the parity sample
     outputs = {(fmt, name): d.cpu().numpy().view(np.uint32) for fmt, name, m, d in launches}
