@@ -62,6 +62,9 @@ struct Model {
 // launchers (stream.cu, gemm.cu, sparse.cu, multiword.cu)
 int launch_block_fma(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c,
                      uint32_t *d, void *stream);
+bool f8_stream_ok(const DevModel &m, int id);
+int launch_block_fma_f8(const DevModel &m, int id, size_t n, const void *a, const void *b, const uint32_t *c,
+                        uint32_t *d, void *stream);
 int launch_tile_gemm(const DevModel &m, int kt, int M, int N, int K, const void *A, int64_t lda,
                      const void *Bt, int64_t ldb, const uint32_t *C, int64_t ldc, uint32_t *D,
                      int64_t ldd, void *stream);

@@ -1,0 +1,256 @@
+// stream_fp8.cu -- block-FMA stream for FP8 operands (E4M3, E5M2; OCP and FNUZ)
+// through a product table.
+//
+// One table read per product replaces two element decodes and a multiplication:
+// the table, indexed by the magnitudes of an operand pair, holds the integer
+// product S_a * S_b, the denormalised product exponent E_a + E_b ("Accurate Models
+// of AMD Matrix Cores", Sec. 4.3.1) and the special-value class of the pair.  The
+// table follows from the format definitions of Table 1 at compile time, lives in
+// global memory, and every CTA copies it into shared memory once (64 KB).  The
+// product sign is the xor of the operand sign bits, taken four products at a time.
+#include <cuda_runtime.h>
+
+#include "core.cuh"
+
+namespace mcemu {
+
+// ---------------------------------------------------------------------------
+// the product table
+// ---------------------------------------------------------------------------
+// Entry (16 bits):
+//   bits 0-7   P = S_a * S_b, 0 when a or b is zero
+//   bit  8     the pair is special and its product is NaN (a NaN operand, or Inf * 0)
+//   bit  9     the pair is special and its product is an infinity
+//   bits 10-15 X = E_a + E_b - XMIN + 1 for a nonzero product, 0 for a zero
+//              product, 63 for a special pair
+// X sits on top, so the largest entry of a block carries e_max (and 63 flags a
+// special pair).  Index: (a & 0x7F) | (b & 0x7F) << 8; bit 7 of the index is unused.
+constexpr int kF8Entries = 32768;
+constexpr uint32_t kF8Special = 63u;
+constexpr int kF8Threads = 512;
+
+template <int ID>
+struct F8 {
+  static constexpr int XMIN = 2 * (1 - Fmt<ID>::BIAS);    // smallest E_a + E_b
+  static constexpr int MAB = 2 * Fmt<ID>::MEFF;           // fraction bits of S_a * S_b
+};
+
+struct F8Table {
+  uint16_t v[kF8Entries];
+};
+
+// class of a 7-bit magnitude: 0 finite, 1 Inf, 2 NaN (FNUZ marks NaN with the sign
+// bit, which the magnitude does not hold; that case is tested on the raw words)
+template <int ID>
+constexpr uint32_t f8_class(uint32_t x) {
+  using F = Fmt<ID>;
+  if (F::FNUZ) return 0u;
+  if (F::E4OCP) return x == 0x7Fu ? 2u : 0u;
+  if (((x >> F::MB) & F::EMASK) != F::EMASK) return 0u;
+  return (x & F::MMASK) ? 2u : 1u;
+}
+
+template <int ID>
+constexpr uint16_t f8_entry(uint32_t a, uint32_t b) {
+  using F = Fmt<ID>;
+  const uint32_t ea = (a >> F::MB) & F::EMASK, eb = (b >> F::MB) & F::EMASK;
+  const uint32_t sa = ea ? ((a & F::MMASK) | (1u << F::MB)) : (a & F::MMASK);
+  const uint32_t sb = eb ? ((b & F::MMASK) | (1u << F::MB)) : (b & F::MMASK);
+  const uint32_t ca = f8_class<ID>(a), cb = f8_class<ID>(b);
+  if (ca || cb) {
+    const bool nan = ca == 2u || cb == 2u || (ca == 1u && sb == 0u) || (cb == 1u && sa == 0u);
+    return (uint16_t)((kF8Special << 10) | (nan ? 0x100u : 0x200u));
+  }
+  const int Ea = (int)(ea ? ea : 1u) - F::BIAS, Eb = (int)(eb ? eb : 1u) - F::BIAS;
+  const uint32_t P = sa * sb;
+  const uint32_t X = P ? (uint32_t)(Ea + Eb - F8<ID>::XMIN + 1) : 0u;
+  return (uint16_t)(P | (X << 10));
+}
+
+template <int ID>
+constexpr F8Table f8_make_table() {
+  F8Table t{};
+  for (uint32_t b = 0; b < 128u; b++)
+    for (uint32_t a = 0; a < 128u; a++) t.v[a | (b << 8)] = f8_entry<ID>(a, b);
+  return t;
+}
+
+__device__ constexpr F8Table kF8TabE4M3 = f8_make_table<F_E4M3>();
+__device__ constexpr F8Table kF8TabE4M3Z = f8_make_table<F_E4M3Z>();
+__device__ constexpr F8Table kF8TabE5M2 = f8_make_table<F_E5M2>();
+__device__ constexpr F8Table kF8TabE5M2Z = f8_make_table<F_E5M2Z>();
+
+template <int ID>
+__device__ __forceinline__ const F8Table &f8_table() {
+  if constexpr (ID == F_E4M3) return kF8TabE4M3;
+  else if constexpr (ID == F_E4M3Z) return kF8TabE4M3Z;
+  else if constexpr (ID == F_E5M2) return kF8TabE5M2;
+  else return kF8TabE5M2Z;
+}
+
+// byte permute (PTX prmt, generic mode): a selector nibble 8 + j copies the sign
+// bit of source byte j into all eight bits of the result byte
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "n"(SEL));
+  return r;
+}
+
+// entries and sign masks (0 or all ones) of the K products of one vector set
+template <int K>
+__device__ __forceinline__ void f8_lookup(const uint16_t *tab, const uint32_t (&wa)[K / 4],
+                                          const uint32_t (&wb)[K / 4], uint32_t (&e)[K], uint32_t (&sg)[K]) {
+#pragma unroll
+  for (int w = 0; w < K / 4; w++) {
+    const uint32_t ma = wa[w] & 0x7F7F7F7Fu, mb = wb[w] & 0x7F7F7F7Fu, xs = wa[w] ^ wb[w];
+    // index of product i: byte i of ma, byte i of mb, then two zero bytes (the
+    // replicated sign bit of byte 0 of ma, which the mask cleared)
+    e[4 * w + 0] = tab[prmt<0x8840u>(ma, mb)];
+    e[4 * w + 1] = tab[prmt<0x8851u>(ma, mb)];
+    e[4 * w + 2] = tab[prmt<0x8862u>(ma, mb)];
+    e[4 * w + 3] = tab[prmt<0x8873u>(ma, mb)];
+    sg[4 * w + 0] = prmt<0x8888u>(xs, xs);
+    sg[4 * w + 1] = prmt<0x9999u>(xs, xs);
+    sg[4 * w + 2] = prmt<0xAAAAu>(xs, xs);
+    sg[4 * w + 3] = prmt<0xBBBBu>(xs, xs);
+  }
+}
+
+// result of a block with a special operand (1 NaN, 2 +Inf, 4 -Inf as in core.cuh)
+template <int ID, int K>
+__device__ __forceinline__ uint32_t f8_special(const DevModel &m, const uint32_t (&e)[K], const uint32_t (&sg)[K],
+                                            uint32_t cb, uint32_t fnuz_nan) {
+  uint32_t s = c_special(cb) | (fnuz_nan ? 1u : 0u);
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if ((e[l] >> 10) == kF8Special) s |= (e[l] & 0x100u) ? 1u : ((sg[l] & 1u) ? 4u : 2u);
+  return resolve_special(m, s);
+}
+
+// Early-c global alignment (Table 3): e_max over the products, c and e_min^lim;
+// each term truncated to F_p fraction bits at e_max, summed exactly, rounded once.
+template <int ID, int K>
+__device__ __forceinline__ uint32_t f8_ga_early(const DevModel &m, const uint32_t (&e)[K], const uint32_t (&sg)[K],
+                                                uint32_t cb, uint32_t mx) {
+  uint32_t cS, cneg;
+  int32_t cE;
+  decode_c(m, cb, cS, cE, cneg);
+  int32_t emax = mx ? (int32_t)(mx >> 10) + F8<ID>::XMIN - 1 : kNegE;
+  const int32_t ec = cS ? cE : m.c_zero_exp;
+  emax = max(max(emax, ec), m.emin_lim);
+  // term l = (P << P0) >> (e_max + R0 - e_l) = (entry << 24) >> (C0 - X_l), and
+  // C0 - X_l = ((C0 << 10 | 0x3FF) - entry) >> 10 since the low ten bits hold P
+  const uint32_t C0s = ((uint32_t)(24 - m.P0 + m.R0 + emax - F8<ID>::XMIN + 1) << 10) | 0x3FFu;
+  int32_t S = 0;
+#pragma unroll
+  for (int l = 0; l < K; l++) {
+    const uint32_t t = shr32(e[l] << 24, (int32_t)((C0s - e[l]) >> 10));
+    S += (int32_t)((t ^ sg[l]) - sg[l]);
+  }
+  if (cS) S += align_term<uint32_t, int32_t>(cS << m.P0c, cneg, emax + m.R0c - cE, 0);
+  if (S == 0) {
+    // a negative zero needs every product to be a negative zero and c = -0
+    uint32_t all = cS == 0u && cneg && mx == 0u ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+    for (int l = 0; l < K; l++) all &= sg[l];
+    return all ? 0x80000000u : 0u;
+  }
+  return pack_sum<int32_t>(S, emax - m.F, m);
+}
+
+template <int ARCH, int ID, int K>
+__global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant__ DevModel m, size_t n,
+                                                           const uint8_t *__restrict__ a,
+                                                           const uint8_t *__restrict__ b,
+                                                           const uint32_t *__restrict__ c,
+                                                           uint32_t *__restrict__ d) {
+  extern __shared__ uint4 f8_smem[];
+  {
+    const uint4 *src = reinterpret_cast<const uint4 *>(f8_table<ID>().v);
+    for (int i = threadIdx.x; i < (int)(sizeof(F8Table) / sizeof(uint4)); i += blockDim.x) f8_smem[i] = src[i];
+  }
+  __syncthreads();
+  const uint16_t *tab = reinterpret_cast<const uint16_t *>(f8_smem);
+  constexpr int NW = K / 4;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
+    uint32_t wa[NW], wb[NW];
+#pragma unroll
+    for (int w = 0; w < NW; w += 2) {
+      const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(a + v * K) + w / 2);
+      const uint2 y = __ldcs(reinterpret_cast<const uint2 *>(b + v * K) + w / 2);
+      wa[w] = x.x; wa[w + 1] = x.y;
+      wb[w] = y.x; wb[w + 1] = y.y;
+    }
+    const uint32_t cb = __ldcs(c + v);
+    uint32_t e[K], sg[K];
+    f8_lookup<K>(tab, wa, wb, e, sg);
+    uint32_t mx = 0;
+#pragma unroll
+    for (int l = 0; l < K; l++) mx = max(mx, e[l]);
+    uint32_t fnuz_nan = 0;
+    if constexpr (Fmt<ID>::FNUZ) {
+#pragma unroll
+      for (int w = 0; w < NW; w++) fnuz_nan |= fspecial_word<ID>(wa[w]) | fspecial_word<ID>(wb[w]);
+    }
+    uint32_t r;
+    if ((mx >> 10) == kF8Special || (cb & 0x7F800000u) == 0x7F800000u || fnuz_nan)
+      r = f8_special<ID, K>(m, e, sg, cb, fnuz_nan);
+    else
+      r = f8_ga_early<ID, K>(m, e, sg, cb, mx);
+    __stcs(d + v, r);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launcher
+// ---------------------------------------------------------------------------
+// true when the table kernel implements the model: FP8 operands of one format,
+// early-c global alignment with truncation, subnormals kept, 32-bit sums
+bool f8_stream_ok(const DevModel &m, int id) {
+  if (id != F_E4M3 && id != F_E4M3Z && id != F_E5M2 && id != F_E5M2Z) return false;
+  if (m.arch != MCEMU_ARCH_GA_EARLY || m.align_rd || m.wide) return false;
+  if (m.fa.sub_keep == 0u || m.c_sub_keep == 0u || m.sub_out_flush) return false;
+  if (m.k != 8 && m.k != 16 && m.k != 32) return false;
+  return m.P0 <= 24;
+}
+
+template <int ARCH, int ID, int K>
+static int f8_run(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c, uint32_t *d,
+                  cudaStream_t s) {
+  auto kern = f8_kernel<ARCH, ID, K>;
+  const int shm = (int)sizeof(F8Table);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, shm) != cudaSuccess)
+    return MCEMU_ERR_CUDA;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kF8Threads, shm);
+  if (per_sm < 1) per_sm = 1;
+  size_t want = (n + kF8Threads - 1) / kF8Threads, full = (size_t)sms * per_sm;
+  const int grid = (int)(want < full ? want : full);
+  kern<<<grid, kF8Threads, shm, s>>>(m, n, (const uint8_t *)a, (const uint8_t *)b, c, d);
+  return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
+}
+
+template <int ID>
+static int f8_run_k(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c, uint32_t *d,
+                    cudaStream_t s) {
+  if (m.k == 8) return f8_run<MCEMU_ARCH_GA_EARLY, ID, 8>(m, n, a, b, c, d, s);
+  if (m.k == 16) return f8_run<MCEMU_ARCH_GA_EARLY, ID, 16>(m, n, a, b, c, d, s);
+  return f8_run<MCEMU_ARCH_GA_EARLY, ID, 32>(m, n, a, b, c, d, s);
+}
+
+int launch_block_fma_f8(const DevModel &m, int id, size_t n, const void *a, const void *b, const uint32_t *c,
+                        uint32_t *d, void *stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  switch (id) {
+    case F_E4M3: return f8_run_k<F_E4M3>(m, n, a, b, c, d, s);
+    case F_E4M3Z: return f8_run_k<F_E4M3Z>(m, n, a, b, c, d, s);
+    case F_E5M2: return f8_run_k<F_E5M2>(m, n, a, b, c, d, s);
+    default: return f8_run_k<F_E5M2Z>(m, n, a, b, c, d, s);
+  }
+}
+
+}  // namespace mcemu
