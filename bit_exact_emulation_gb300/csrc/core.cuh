@@ -822,6 +822,10 @@ __device__ __forceinline__ Term<UT> fterm(uint32_t a, uint32_t b, uint32_t sub_k
   return t;
 }
 
+template <int ID>
+__device__ __forceinline__ uint32_t exact_fixed_merge(const DevModel &m, i128 W, uint32_t cS, int32_t cE,
+                                                      uint32_t cneg, uint32_t cbits);
+
 // Exact-then-round for formats whose products lie on one fixed grid (fp16, fp8):
 // every product is a multiple of 2^Lp, Lp = 2 (e_min - m), and below 2^(Tp + log2 K),
 // so the exact product sum P fits a 128-bit window with LSB L = Lp - 40.  The addend
@@ -843,10 +847,18 @@ __device__ __forceinline__ uint32_t arch_exact_fixed(const DevModel &m, const Te
     const i128 v = (i128)((u128)p[l].U << (p[l].U ? sh : 0));
     W += p[l].neg ? -v : v;
   }
-  if (cS == 0) {
-    if (W == 0) return zero_result<K, uint32_t>(p, K, cS, cneg);
-    return round_pack128(W, L, false, m);
-  }
+  if (cS == 0 && W == 0) return zero_result<K, uint32_t>(p, K, cS, cneg);
+  return exact_fixed_merge<ID>(m, W, cS, cE, cneg, cbits);
+}
+
+// The addend step of arch_exact_fixed: W (units of 2^L, L = Lp - 40) is the exact
+// product sum, not zero unless c is.
+template <int ID>
+__device__ __forceinline__ uint32_t exact_fixed_merge(const DevModel &m, i128 W, uint32_t cS, int32_t cE,
+                                                      uint32_t cneg, uint32_t cbits) {
+  using F = Fmt<ID>;
+  constexpr int32_t L = 2 * (1 - F::BIAS - F::MEFF) - 40;
+  if (cS == 0) return round_pack128(W, L, false, m);
   if (W == 0) return cbits;                          // c alone: already an fp32 value
   const int32_t lc = cE - 23;                        // c = +-S_c * 2^lc, S_c < 2^24
   const int64_t vc = cneg ? -(int64_t)cS : (int64_t)cS;

@@ -1,5 +1,5 @@
 // stream_fp8.cu -- block-FMA stream for FP8 operands (E4M3, E5M2; OCP and FNUZ)
-// through a product table.
+// through a product table: early-c global alignment and exact-then-round.
 //
 // One table read per product replaces two element decodes and a multiplication:
 // the table, indexed by the magnitudes of an operand pair, holds the integer
@@ -117,20 +117,36 @@ __device__ __forceinline__ void f8_lookup(const uint16_t *tab, const uint32_t (&
   }
 }
 
-// result of a block with a special operand (1 NaN, 2 +Inf, 4 -Inf as in core.cuh)
+// Result of a block with a special operand (1 NaN, 2 +Inf, 4 -Inf as in core.cuh).
+// `orv` is the OR of the entries: bit 8 some product is NaN, bit 9 some is infinite.
 template <int ID, int K>
 __device__ __forceinline__ uint32_t f8_special(const DevModel &m, const uint32_t (&e)[K], const uint32_t (&sg)[K],
-                                            uint32_t cb, uint32_t fnuz_nan) {
-  uint32_t s = c_special(cb) | (fnuz_nan ? 1u : 0u);
+                                               uint32_t orv, uint32_t cb, uint32_t fnuz_nan) {
+  uint32_t s = c_special(cb) | (fnuz_nan || (orv & 0x100u) ? 1u : 0u);
+  if (s == 0u || (s & 6u)) {          // infinite products: their signs matter
+    if (orv & 0x200u) {
 #pragma unroll
-  for (int l = 0; l < K; l++)
-    if ((e[l] >> 10) == kF8Special) s |= (e[l] & 0x100u) ? 1u : ((sg[l] & 1u) ? 4u : 2u);
+      for (int l = 0; l < K; l++)
+        if (e[l] & 0x200u) s |= (sg[l] & 1u) ? 4u : 2u;
+    }
+  }
   return resolve_special(m, s);
+}
+
+// fp32 bits of S * 2^k, S != 0 an integer, rounded (RNE or RZ) in hardware; false
+// when the result is subnormal or k is out of the single-multiply range
+template <bool RNE>
+__device__ __forceinline__ bool f8_round(int32_t S, int32_t k, uint32_t &bits) {
+  if ((uint32_t)(k + 126) > 253u) return false;
+  const float x = RNE ? __int2float_rn(S) : __int2float_rz(S);
+  const float sc = __uint_as_float((uint32_t)(k + 127) << 23);
+  bits = __float_as_uint(RNE ? __fmul_rn(x, sc) : __fmul_rz(x, sc));
+  return (bits & 0x7F800000u) != 0u;
 }
 
 // Early-c global alignment (Table 3): e_max over the products, c and e_min^lim;
 // each term truncated to F_p fraction bits at e_max, summed exactly, rounded once.
-template <int ID, int K>
+template <int ID, int K, bool RNE>
 __device__ __forceinline__ uint32_t f8_ga_early(const DevModel &m, const uint32_t (&e)[K], const uint32_t (&sg)[K],
                                                 uint32_t cb, uint32_t mx) {
   uint32_t cS, cneg;
@@ -156,10 +172,62 @@ __device__ __forceinline__ uint32_t f8_ga_early(const DevModel &m, const uint32_
     for (int l = 0; l < K; l++) all &= sg[l];
     return all ? 0x80000000u : 0u;
   }
+  uint32_t bits;
+  if (f8_round<RNE>(S, emax - m.F, bits)) return bits;
   return pack_sum<int32_t>(S, emax - m.F, m);
 }
 
-template <int ARCH, int ID, int K>
+// Exact-then-round (CDNA 1): every product is +-P * 2^X on the grid 2^G with
+// G = XMIN - MAB - 1.  E4M3 sums fit one 64-bit accumulator; E5M2 products span
+// 2^0 .. 2^66 on that grid and are split at 2^31 into two.  The addend and the single
+// rounding follow arch_exact_fixed, on the same 2^(G - 39) window.
+__device__ __forceinline__ int64_t mad_wide(int32_t a, int32_t b, int64_t c) {
+  int64_t r;
+  asm("mad.wide.s32 %0, %1, %2, %3;" : "=l"(r) : "r"(a), "r"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint32_t shl_clamp(uint32_t x, uint32_t s) {   // 0 once s >= 32
+  uint32_t r;
+  asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(s));
+  return r;
+}
+
+template <int ID, int K>
+__device__ __forceinline__ uint32_t f8_exact(const DevModel &m, const uint32_t (&e)[K], const uint32_t (&sg)[K],
+                                             uint32_t cb, uint32_t mx) {
+  i128 W;
+  if constexpr (Fmt<ID>::EB == 4) {
+    int64_t w = 0;
+#pragma unroll
+    for (int l = 0; l < K; l++) {
+      const int32_t sP = (int32_t)(((e[l] & 0xFFu) ^ sg[l]) - sg[l]);
+      w = mad_wide(sP, (int32_t)shl_clamp(1u, e[l] >> 10), w);      // X <= 29
+    }
+    W = (i128)w;
+  } else {
+    int64_t lo = 0, hi = 0;
+#pragma unroll
+    for (int l = 0; l < K; l++) {
+      const uint32_t X = e[l] >> 10;
+      const int32_t sP = (int32_t)(((e[l] & 0xFFu) ^ sg[l]) - sg[l]);
+      lo = mad_wide(sP, (int32_t)(shl_clamp(2u, X) >> 1), lo);      // 2^X for X <= 30, else 0
+      hi = mad_wide(sP, (int32_t)shl_clamp(1u, X - 31u), hi);       // 2^(X-31) for X >= 31, else 0
+    }
+    W = (i128)lo + ((i128)hi << 31);
+  }
+  uint32_t cS, cneg;
+  int32_t cE;
+  decode_c(m, cb, cS, cE, cneg);
+  if (cS == 0 && W == 0) {
+    uint32_t all = cneg && mx == 0u ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+    for (int l = 0; l < K; l++) all &= sg[l];
+    return all ? 0x80000000u : 0u;
+  }
+  return exact_fixed_merge<ID>(m, W << 39, cS, cE, cneg, cb);
+}
+
+template <int ARCH, int ID, int K, bool RNE>
 __global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant__ DevModel m, size_t n,
                                                            const uint8_t *__restrict__ a,
                                                            const uint8_t *__restrict__ b,
@@ -186,19 +254,24 @@ __global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant
     const uint32_t cb = __ldcs(c + v);
     uint32_t e[K], sg[K];
     f8_lookup<K>(tab, wa, wb, e, sg);
-    uint32_t mx = 0;
+    uint32_t mx = 0, orv = 0;
 #pragma unroll
-    for (int l = 0; l < K; l++) mx = max(mx, e[l]);
+    for (int l = 0; l < K; l++) {
+      mx = max(mx, e[l]);
+      orv |= e[l];
+    }
     uint32_t fnuz_nan = 0;
     if constexpr (Fmt<ID>::FNUZ) {
 #pragma unroll
       for (int w = 0; w < NW; w++) fnuz_nan |= fspecial_word<ID>(wa[w]) | fspecial_word<ID>(wb[w]);
     }
     uint32_t r;
-    if ((mx >> 10) == kF8Special || (cb & 0x7F800000u) == 0x7F800000u || fnuz_nan)
-      r = f8_special<ID, K>(m, e, sg, cb, fnuz_nan);
+    if ((orv & 0x300u) || (cb & 0x7F800000u) == 0x7F800000u || fnuz_nan)
+      r = f8_special<ID, K>(m, e, sg, orv, cb, fnuz_nan);
+    else if constexpr (ARCH == MCEMU_ARCH_GA_EARLY)
+      r = f8_ga_early<ID, K, RNE>(m, e, sg, cb, mx);
     else
-      r = f8_ga_early<ID, K>(m, e, sg, cb, mx);
+      r = f8_exact<ID, K>(m, e, sg, cb, mx);
     __stcs(d + v, r);
   }
 }
@@ -207,19 +280,20 @@ __global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant
 // launcher
 // ---------------------------------------------------------------------------
 // true when the table kernel implements the model: FP8 operands of one format,
-// early-c global alignment with truncation, subnormals kept, 32-bit sums
+// early-c global alignment with truncation and 32-bit sums, or exact-then-round;
+// subnormals kept
 bool f8_stream_ok(const DevModel &m, int id) {
   if (id != F_E4M3 && id != F_E4M3Z && id != F_E5M2 && id != F_E5M2Z) return false;
-  if (m.arch != MCEMU_ARCH_GA_EARLY || m.align_rd || m.wide) return false;
   if (m.fa.sub_keep == 0u || m.c_sub_keep == 0u || m.sub_out_flush) return false;
   if (m.k != 8 && m.k != 16 && m.k != 32) return false;
-  return m.P0 <= 24;
+  if (m.arch == MCEMU_ARCH_EXACT) return true;
+  return m.arch == MCEMU_ARCH_GA_EARLY && !m.align_rd && !m.wide && m.P0 <= 24;
 }
 
-template <int ARCH, int ID, int K>
+template <int ARCH, int ID, int K, bool RNE>
 static int f8_run(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c, uint32_t *d,
                   cudaStream_t s) {
-  auto kern = f8_kernel<ARCH, ID, K>;
+  auto kern = f8_kernel<ARCH, ID, K, RNE>;
   const int shm = (int)sizeof(F8Table);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, shm) != cudaSuccess)
     return MCEMU_ERR_CUDA;
@@ -234,22 +308,30 @@ static int f8_run(const DevModel &m, size_t n, const void *a, const void *b, con
   return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
 }
 
-template <int ID>
+template <int ARCH, int ID, bool RNE>
 static int f8_run_k(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c, uint32_t *d,
                     cudaStream_t s) {
-  if (m.k == 8) return f8_run<MCEMU_ARCH_GA_EARLY, ID, 8>(m, n, a, b, c, d, s);
-  if (m.k == 16) return f8_run<MCEMU_ARCH_GA_EARLY, ID, 16>(m, n, a, b, c, d, s);
-  return f8_run<MCEMU_ARCH_GA_EARLY, ID, 32>(m, n, a, b, c, d, s);
+  if (m.k == 8) return f8_run<ARCH, ID, 8, RNE>(m, n, a, b, c, d, s);
+  if (m.k == 16) return f8_run<ARCH, ID, 16, RNE>(m, n, a, b, c, d, s);
+  return f8_run<ARCH, ID, 32, RNE>(m, n, a, b, c, d, s);
+}
+
+template <int ID>
+static int f8_run_id(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c, uint32_t *d,
+                     cudaStream_t s) {
+  if (m.arch == MCEMU_ARCH_EXACT) return f8_run_k<MCEMU_ARCH_EXACT, ID, true>(m, n, a, b, c, d, s);
+  if (m.rne) return f8_run_k<MCEMU_ARCH_GA_EARLY, ID, true>(m, n, a, b, c, d, s);
+  return f8_run_k<MCEMU_ARCH_GA_EARLY, ID, false>(m, n, a, b, c, d, s);
 }
 
 int launch_block_fma_f8(const DevModel &m, int id, size_t n, const void *a, const void *b, const uint32_t *c,
                         uint32_t *d, void *stream) {
   cudaStream_t s = (cudaStream_t)stream;
   switch (id) {
-    case F_E4M3: return f8_run_k<F_E4M3>(m, n, a, b, c, d, s);
-    case F_E4M3Z: return f8_run_k<F_E4M3Z>(m, n, a, b, c, d, s);
-    case F_E5M2: return f8_run_k<F_E5M2>(m, n, a, b, c, d, s);
-    default: return f8_run_k<F_E5M2Z>(m, n, a, b, c, d, s);
+    case F_E4M3: return f8_run_id<F_E4M3>(m, n, a, b, c, d, s);
+    case F_E4M3Z: return f8_run_id<F_E4M3Z>(m, n, a, b, c, d, s);
+    case F_E5M2: return f8_run_id<F_E5M2>(m, n, a, b, c, d, s);
+    default: return f8_run_id<F_E5M2Z>(m, n, a, b, c, d, s);
   }
 }
 
