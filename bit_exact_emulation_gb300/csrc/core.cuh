@@ -553,6 +553,74 @@ __device__ __forceinline__ uint32_t arch_exact(const DevModel &m, const Term<UT>
   return r;
 }
 
+// EXACT with a 64-bit window, for products of at most 22 significant bits (FP16,
+// BF16, XF32) and an fp32 c.  T bounds the top bit of every term; the window holds
+// units of 2^L with L = T - 61 + ceil(log2(K + 1)), so the K + 1 terms sum below
+// 2^61.  A term +-v * 2^lsb (|v| < 2^wid) is placed as (v << Q) >> r with the
+// constant Q = 62 - wid and r = Q - lsb + L >= 0: one arithmetic shift floors it
+// into the window and the bits it drops set the sticky count nb.  The true sum then
+// lies in [W, W + nb) units, excluding W itself when nb > 0.  With |W| >= 2^26 the
+// rounding boundaries of that range are multiples of 4 units, so W + 1/4 and
+// W + nb - 1/4 (4W + 1 and 4(W + nb) - 1 in units of 2^(L-2)) round like every value
+// the sum can take next to them: when both give the same fp32 value, that value is
+// the correctly rounded sum.  Otherwise (heavy cancellation, or a subnormal result)
+// the full-width evaluator decides.
+template <int K>
+struct ExactLog {
+  static constexpr int v = K + 1 <= 2 ? 1 : K + 1 <= 4 ? 2 : K + 1 <= 8 ? 3 : K + 1 <= 16 ? 4 : K + 1 <= 32 ? 5 : 6;
+};
+
+template <int K>
+__device__ __forceinline__ void exact64_add(int64_t &W, int32_t &nb, int32_t sv, int32_t Q, int32_t r) {
+  // sv * 2^Q has zero low 32 bits (Q >= 32), so only bits of the high word drop out
+  const int64_t V = (int64_t)((uint64_t)((uint32_t)sv << (Q - 32)) << 32);
+  const int32_t rr = min(r, 63);
+  W += V >> rr;
+  const uint32_t hi = (uint32_t)(V >> 32);
+  nb += (rr > 32 && (hi << (64 - rr)) != 0u) ? 1 : 0;
+}
+
+template <int K, class UT>
+__device__ __forceinline__ uint32_t arch_exact64(const DevModel &m, const Term<UT> (&p)[K], uint32_t cS,
+                                                 int32_t cE, uint32_t cneg) {
+  int32_t T = kNegE;
+#pragma unroll
+  for (int l = 0; l < K; l++) T = max(T, p[l].e + 2);
+  if (cS) T = max(T, cE + 1);
+  if (T <= kNegE / 2) return zero_result<K, UT>(p, K, cS, cneg);
+  const int32_t L = T - 61 + ExactLog<K>::v;
+  const int32_t QP = 60 - m.mab;                     // products: |U| < 2^(mab + 2)
+  int64_t W = 0;
+  int32_t nb = 0;
+#pragma unroll
+  for (int l = 0; l < K; l++) {
+    const int32_t sv = p[l].neg ? -(int32_t)p[l].U : (int32_t)p[l].U;
+    exact64_add<K>(W, nb, sv, QP, QP - (p[l].e - m.mab) + L);
+  }
+  if (cS) exact64_add<K>(W, nb, cneg ? -(int32_t)cS : (int32_t)cS, 38, 38 - (cE - 23) + L);
+  uint32_t lo, hi;
+  if (nb == 0) {
+    if (W == 0) return zero_result<K, UT>(p, K, cS, cneg);
+    if (hw_round64(W, L, m.rne, lo) && !m.sub_out_flush) return lo;
+  } else if (!m.sub_out_flush && (W >= (1ll << 26) || W <= -(1ll << 26)) && hw_round64(4 * W + 1, L - 2, m.rne, lo) &&
+             hw_round64(4 * (W + nb) - 1, L - 2, m.rne, hi) && lo == hi) {
+    return lo;
+  }
+  int64_t V[K + 1];
+  int32_t Ls[K + 1];
+  int n = 0;
+#pragma unroll
+  for (int l = 0; l < K; l++) {
+    V[n] = p[l].neg ? -(int64_t)p[l].U : (int64_t)p[l].U;
+    Ls[n] = p[l].e - m.mab;
+    n++;
+  }
+  V[n] = cneg ? -(int64_t)cS : (int64_t)cS;
+  Ls[n] = cE - 23;
+  n++;
+  return exact_slow(m, V, Ls, n);
+}
+
 // ---------------------------------------------------------------------------
 // PAIRWISE: fl(c + fl(fl(p1+p2) + fl(p3+p4))), fl = RNE to fp32 with optional
 // subnormal flush after every operation (Sec. 4.2).  IEEE fp32 hardware
@@ -925,8 +993,10 @@ __device__ __forceinline__ uint32_t block_fma_fast(const DevModel &m, const uint
   if constexpr (ARCH == MCEMU_ARCH_GA_EARLY) return arch_ga_early<K, UT, AT>(m, p, K, cS, cE, cneg);
   else if constexpr (ARCH == MCEMU_ARCH_GA_LATE) return arch_ga_late<K, UT, AT>(m, p, K, cS, cE, cneg);
   else if constexpr (ARCH == MCEMU_ARCH_ODD_EVEN) return arch_odd_even<K, UT, AT>(m, p, K, cS, cE, cneg);
-  else if constexpr (ID == F_FP16 || ID == F_E4M3 || ID == F_E4M3Z || ID == F_E5M2 || ID == F_E5M2Z)
+  else if constexpr (ID == F_E4M3 || ID == F_E4M3Z || ID == F_E5M2 || ID == F_E5M2Z)
     return arch_exact_fixed<ID, K>(m, p, cS, cE, cneg, cbits);
+  else if constexpr (ID == F_FP16 || ID == F_BF16 || ID == F_XF32T || ID == F_XF32R)
+    return arch_exact64<K, UT>(m, p, cS, cE, cneg);
   else return arch_exact<K, UT>(m, p, K, cS, cE, cneg);
 }
 

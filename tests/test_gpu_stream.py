@@ -143,6 +143,49 @@ def test_cdna3_exponent_mantissa_sampling(L, preset, fmt, eab, ec):
     assert np.array_equal(got, want), preset + "\n" + mismatches(got, want, a, b, c)
 
 
+def _cancellation_set(fmt, n, seed):
+    """K=4 vector sets built to stress exact-then-round: c nearly cancels the first
+    product, the other products sit 10-40 and 50-110 binades lower, so the sum keeps
+    few bits above the far terms and sticky information decides the rounding."""
+    rng = np.random.default_rng(seed)
+    to_bits = {"bf16": lambda x: W.fp32_to_bf16_rne(x.astype(np.float32)),
+               "fp16": lambda x: x.astype(np.float16).view(np.uint16),
+               "xf32": lambda x: (x.astype(np.float32).view(np.uint32) & np.uint32(0xFFFFE000))}[fmt]
+    lo = {"bf16": (-60, -110), "fp16": (-10, -22), "xf32": (-60, -110)}[fmt]
+
+    def vals(e_lo, e_hi, size):
+        return rng.uniform(1, 2, size) * np.exp2(rng.integers(e_lo, e_hi + 1, size)) * rng.choice([-1, 1], size)
+
+    a = np.empty((n, 4), dtype=W.ELEM_DTYPE[fmt])
+    b = np.empty((n, 4), dtype=W.ELEM_DTYPE[fmt])
+    a[:, 0], b[:, 0] = to_bits(vals(0, 0, n)), to_bits(vals(0, 0, n))
+    half = 5 if fmt == "fp16" else 20
+    a[:, 1], b[:, 1] = to_bits(vals(-half, -3, n)), to_bits(vals(-half, -3, n))
+    a[:, 2], b[:, 2] = to_bits(vals(lo[1] // 2, lo[0] // 2, n)), to_bits(vals(lo[1] // 2, lo[0] // 2, n))
+    a[:, 3], b[:, 3] = to_bits(vals(-half, -2, n)), to_bits(vals(-half, -2, n))
+    a[n // 2:, 3] = 0                                   # half of them without the fourth product
+    # c: minus the first product rounded to fp32, moved by a few units in the last place
+    if fmt == "bf16":
+        fa = (a[:, 0].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        fb = (b[:, 0].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    elif fmt == "fp16":
+        fa, fb = a[:, 0].view(np.float16).astype(np.float64), b[:, 0].view(np.float16).astype(np.float64)
+    else:
+        fa, fb = a[:, 0].view(np.float32).astype(np.float64), b[:, 0].view(np.float32).astype(np.float64)
+    c = (-(fa * fb)).astype(np.float32).view(np.int32) + rng.integers(-3, 4, n).astype(np.int32)
+    return a, b, c.view(np.uint32)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp16", "xf32"])
+def test_exact_cancellation_and_sticky(L, fmt):
+    a, b, c = _cancellation_set(fmt, 100000, seed=17)
+    for name in ("ieee_exact", "ga_rne", "ga_trunc"):
+        spec = block_models(fmt, 4)[name] if fmt != "xf32" else dict(block_models("xf32", 2)[name], n_fma=4)
+        got = gpu_block(L, spec, a, b, c)
+        want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+        assert np.array_equal(got, want), f"{fmt} {name}\n" + mismatches(got, want, a, b, c)
+
+
 GENERIC_CASES = [
     ("exact", "fp16", 1), ("exact", "bf16", 3), ("ga_early", "bf16", 5), ("ga_late", "fp16", 12),
     ("odd_even", "e4m3", 32), ("ga_early", "e5m2", 32), ("pairwise", "bf16", 8), ("exact", "xf32", 16),
