@@ -580,6 +580,30 @@ __device__ __forceinline__ void exact64_add(int64_t &W, int32_t &nb, int32_t sv,
   nb += (rr > 32 && (hi << (64 - rr)) != 0u) ? 1 : 0;
 }
 
+// Correct rounding of Wt * 2^Gw (plus an unknown amount in (0, 2^Gw) when stW) plus
+// c, for Wt != 0 with |Wt| < 2^62: both terms are floored into a 64-bit window under
+// the larger one and rounded through the same bracket as arch_exact64.  False when
+// the bracket does not decide (the caller then takes an exact path).
+__device__ __forceinline__ bool merge_c64(const DevModel &m, int64_t Wt, int32_t Gw, int32_t stW, uint32_t cS,
+                                          int32_t cE, uint32_t cneg, uint32_t &out) {
+  const uint64_t aw = Wt < 0 ? (uint64_t)(-Wt) : (uint64_t)Wt;
+  int32_t T = Gw + 64 - __clzll((long long)aw);      // |W| < 2^T
+  if (cS) T = max(T, cE + 1);
+  const int32_t L = T - 60;                          // two terms: |sum| < 2^61 units
+  const int32_t left = max(Gw - L, 0), right = min(max(L - Gw, 0), 63);
+  const int64_t Wl = (int64_t)((uint64_t)Wt << left);
+  int64_t S = Wl >> right;
+  int32_t nb = stW + ((right > 0 && (Wl & (int64_t)((1ull << right) - 1ull)) != 0) ? 1 : 0);
+  if (cS) exact64_add<1>(S, nb, cneg ? -(int32_t)cS : (int32_t)cS, 38, 38 - (cE - 23) + L);
+  if (nb == 0) {
+    if (S == 0) { out = 0u; return true; }             // exact cancellation: +0
+    return hw_round64(S, L, m.rne, out);
+  }
+  uint32_t hi;
+  return (S >= (1ll << 26) || S <= -(1ll << 26)) && hw_round64(4 * S + 1, L - 2, m.rne, out) &&
+         hw_round64(4 * (S + nb) - 1, L - 2, m.rne, hi) && out == hi;
+}
+
 template <int K, class UT>
 __device__ __forceinline__ uint32_t arch_exact64(const DevModel &m, const Term<UT> (&p)[K], uint32_t cS,
                                                  int32_t cE, uint32_t cneg) {

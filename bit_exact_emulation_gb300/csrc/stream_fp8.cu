@@ -218,12 +218,29 @@ __device__ __forceinline__ uint32_t f8_exact(const DevModel &m, const uint32_t (
   uint32_t cS, cneg;
   int32_t cE;
   decode_c(m, cb, cS, cE, cneg);
-  if (cS == 0 && W == 0) {
+  if (W == 0) {
+    if (cS) return cb;                                  // c alone: already an fp32 value
     uint32_t all = cneg && mx == 0u ? 0xFFFFFFFFu : 0u;
 #pragma unroll
     for (int l = 0; l < K; l++) all &= sg[l];
     return all ? 0x80000000u : 0u;
   }
+  // the exact sum's top 62 bits (all of it for E4M3) and the addend in a 64-bit window
+  constexpr int32_t G = F8<ID>::XMIN - F8<ID>::MAB - 1;
+  int64_t Wt;
+  int32_t Gw = G, stW = 0;
+  if constexpr (Fmt<ID>::EB == 4) {
+    Wt = (int64_t)W;
+  } else {
+    const i128 aW = W < 0 ? -W : W;
+    const uint64_t top = (uint64_t)(aW >> 61);
+    const int32_t sh = top ? 64 - __clzll((long long)top) : 0;   // bits to drop
+    Wt = (int64_t)(W >> sh);
+    stW = (sh > 0 && (W & (((i128)1 << sh) - 1)) != 0) ? 1 : 0;
+    Gw = G + sh;
+  }
+  uint32_t r;
+  if (merge_c64(m, Wt, Gw, stW, cS, cE, cneg, r)) return r;
   return exact_fixed_merge<ID>(m, W << 39, cS, cE, cneg, cb);
 }
 
