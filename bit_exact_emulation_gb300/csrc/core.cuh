@@ -979,6 +979,28 @@ __device__ __forceinline__ uint32_t exact_fixed_merge(const DevModel &m, i128 W,
   return round_pack128(W2, L2, st, m);
 }
 
+// Special-value bits (1 NaN, 2 +Inf, 4 -Inf) of a block with an Inf/NaN operand or
+// addend, format fixed at compile time.
+template <int ID, int K>
+__device__ __forceinline__ uint32_t fspecial_bits(const DevModel &m, const uint32_t (&ea)[K],
+                                                  const uint32_t (&eb)[K], uint32_t cbits) {
+  uint32_t spec = 0;
+  if constexpr (ID == F_FP16 || ID == F_E4M3 || ID == F_E5M2) {
+    // the inputs are exact in fp32 and their products cannot overflow it, so the
+    // IEEE sum c + sum a*b is NaN / +-Inf exactly when the model's result is
+    // (subnormal flushing changes Inf*0 and is not taken on this path)
+    float t = __uint_as_float(cbits);
+#pragma unroll
+    for (int l = 0; l < K; l++) t = __fadd_rn(t, __fmul_rn(felem_float<ID>(ea[l]), felem_float<ID>(eb[l])));
+    if (!(fabsf(t) <= 3.4028235e38f)) spec = (t != t) ? 1u : (t > 0.0f ? 2u : 4u);
+  } else {
+    spec = c_special(cbits);
+#pragma unroll
+    for (int l = 0; l < K; l++) spec |= fprod_special<ID>(ea[l], eb[l], m.fa.sub_keep);
+  }
+  return spec;
+}
+
 // One block FMA of K products, architecture and format fixed at compile time.
 template <int ARCH, int ID, int K, class UT, class AT>
 __device__ __forceinline__ uint32_t block_fma_fast(const DevModel &m, const uint32_t (&ea)[K],
@@ -987,22 +1009,7 @@ __device__ __forceinline__ uint32_t block_fma_fast(const DevModel &m, const uint
   Term<UT> p[K];
 #pragma unroll
   for (int l = 0; l < K; l++) p[l] = fterm<ID, UT>(ea[l], eb[l], sk);
-  uint32_t spec = 0;
-  if (any_special) {
-    if constexpr (ID == F_FP16 || ID == F_E4M3 || ID == F_E5M2) {
-      // the inputs are exact in fp32 and their products cannot overflow it, so the
-      // IEEE sum c + sum a*b is NaN / +-Inf exactly when the model's result is
-      // (subnormal flushing changes Inf*0 and is not taken on this path)
-      float t = __uint_as_float(cbits);
-#pragma unroll
-      for (int l = 0; l < K; l++) t = __fadd_rn(t, __fmul_rn(felem_float<ID>(ea[l]), felem_float<ID>(eb[l])));
-      if (!(fabsf(t) <= 3.4028235e38f)) spec = (t != t) ? 1u : (t > 0.0f ? 2u : 4u);
-    } else {
-      spec = c_special(cbits);
-#pragma unroll
-      for (int l = 0; l < K; l++) spec |= fprod_special<ID>(ea[l], eb[l], sk);
-    }
-  }
+  uint32_t spec = any_special ? fspecial_bits<ID, K>(m, ea, eb, cbits) : 0u;
   if constexpr (ID == F_BF16 || ID == F_XF32T || ID == F_XF32R || ID == F_FP32) {
     if (m.prod_ovf) {
 #pragma unroll
