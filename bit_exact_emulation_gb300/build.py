@@ -11,7 +11,7 @@ from concurrent.futures import ThreadPoolExecutor
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB_PATH = os.path.join(HERE, "libmcemu.so")
-SOURCES = ["api.cu", "stream.cu", "stream_fp8.cu", "gemm.cu", "gemm_fast.cu", "gemm_fast_sw.cu", "sparse.cu", "multiword.cu"]
+SOURCES = ["api.cu", "stream.cu", "stream_fp8.cu", "gemm.cu", "gemm_fast.cu", "gemm_fast_sw.cu", "gemm_exact.cu", "sparse.cu", "multiword.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(HERE, "..", "include")]

@@ -130,6 +130,8 @@ int launch_tile_gemm(const DevModel &m, int kt, int M, int N, int K, const void 
   cudaStream_t s = (cudaStream_t)stream;
   if (kt > 1024) return MCEMU_ERR_UNSUPPORTED;
   if (gemm_fast_ok(m) && kt <= 64) return launch_tile_gemm_fast(m, kt, M, N, K, A, lda, Bt, ldb, C, ldc, D, ldd, stream);
+  if (gemm_exact_ok(m) && kt <= 64)
+    return launch_tile_gemm_exact(m, kt, M, N, K, A, lda, Bt, ldb, C, ldc, D, ldd, stream);
   const size_t shm = (size_t)2 * kT * chunk_len(kt) * 4;
   dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT), block(kT, kT);
   const uint8_t *a = (const uint8_t *)A, *b = (const uint8_t *)Bt;
@@ -158,6 +160,8 @@ int launch_sparse24_gemm(const DevModel &m, int kt, int M, int N, int K, const v
   if (kt > 1024) return MCEMU_ERR_UNSUPPORTED;
   if (sparse_fast_ok(m, kt))
     return launch_sparse24_gemm_fast(m, kt, M, N, K, Ac, ldac, meta, ldm, Bt, ldb, C, ldc, D, ldd, stream);
+  if (gemm_exact_ok(m) && m.k % 2 == 0 && 2 * m.k <= 32 && kt <= 64 && elem_size(m) <= 2)
+    return launch_sparse24_gemm_exact(m, kt, M, N, K, Ac, ldac, meta, ldm, Bt, ldb, C, ldc, D, ldd, stream);
   const int Kc = K / 2, ktc = kt / 2;
   const size_t shm = (size_t)4 * kT * chunk_len(ktc) * 4;
   dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT), block(kT, kT);

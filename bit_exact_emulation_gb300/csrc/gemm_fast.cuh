@@ -48,6 +48,41 @@ __device__ __forceinline__ uint32_t stage_elem(const FmtDev &f, uint32_t x, int3
   return classify(f, x) != 0u ? 1u : 0u;
 }
 
+// Stage one K-chunk of the CTA's A rows and B columns into shared memory, decoded:
+// element (r, q) of the chunk goes to [q][r] as significand, exponent (kZeroE for a
+// zero) and sign +-1; B significands are shifted left by bshift.  A row or column
+// that holds an Inf/NaN (or, for SPARSE, invalid metadata) is flagged.
+template <int ESZ, int SPARSE>
+__device__ __forceinline__ void stage_chunk(const DevModel &m, int bshift, int i0, int j0, int k0, int kc, int KC,
+                                            int M, int N, const uint8_t *__restrict__ A, int64_t lda,
+                                            const uint8_t *__restrict__ meta, int64_t ldm,
+                                            const uint8_t *__restrict__ Bt, int64_t ldb, int32_t *aS, int32_t *aE,
+                                            int32_t *aG, int32_t *bS, int32_t *bE, int32_t *bG, uint8_t *aSpec,
+                                            uint8_t *bSpec) {
+  for (int e = threadIdx.x; e < kFB * KC; e += blockDim.x) {
+    const int r = e / KC, q = e % KC;
+    int32_t S = 0, E = kZeroE, G = 1;
+    if constexpr (SPARSE) {
+      if (i0 + r < M && q < kc) {
+        const int kd = k0 + q, g = kd >> 2, p = kd & 3;
+        const uint32_t mb = meta[(int64_t)(i0 + r) * ldm + g];
+        const uint32_t idx0 = mb & 3u, idx1 = (mb >> 2) & 3u;
+        if (idx0 >= idx1) aSpec[r] = 1;                  // not a valid 2:4 pattern
+        const int t = (p == (int)idx0) ? 0 : (p == (int)idx1) ? 1 : -1;
+        if (t >= 0 && stage_elem(m.fa, fld<ESZ>(A, (int64_t)(i0 + r) * lda + 2 * g + t), S, E, G)) aSpec[r] = 1;
+      }
+    } else {
+      if (i0 + r < M && q < kc && stage_elem(m.fa, fld<ESZ>(A, (int64_t)(i0 + r) * lda + k0 + q), S, E, G))
+        aSpec[r] = 1;
+    }
+    aS[q * kFS + r] = S; aE[q * kFS + r] = E; aG[q * kFS + r] = G;
+    S = 0; E = kZeroE; G = 1;
+    if (j0 + r < N && q < kc && stage_elem(m.fb, fld<ESZ>(Bt, (int64_t)(j0 + r) * ldb + k0 + q), S, E, G))
+      bSpec[r] = 1;
+    bS[q * kFS + r] = S << bshift; bE[q * kFS + r] = E; bG[q * kFS + r] = G;
+  }
+}
+
 // The whole chain of one output with the general evaluator, reading raw operands
 // from global memory (outputs that met a case the fast path leaves out); C == nullptr
 // stands for C = 0.
@@ -206,29 +241,8 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
     __syncthreads();
     if (tid < kFB) { aSpec[tid] = 0; bSpec[tid] = 0; }
     __syncthreads();
-    // stage and decode: element (r, q) of the chunk -> [q][r]
-    for (int e = tid; e < kFB * KC; e += kFThreads) {
-      const int r = e / KC, q = e % KC;
-      int32_t S = 0, E = kZeroE, G = 1;
-      if constexpr (SPARSE) {
-        if (i0 + r < M && q < kc) {
-          const int kd = k0 + q, g = kd >> 2, p = kd & 3;
-          const uint32_t mb = meta[(int64_t)(i0 + r) * ldm + g];
-          const uint32_t idx0 = mb & 3u, idx1 = (mb >> 2) & 3u;
-          if (idx0 >= idx1) aSpec[r] = 1;                  // not a valid 2:4 pattern
-          const int t = (p == (int)idx0) ? 0 : (p == (int)idx1) ? 1 : -1;
-          if (t >= 0 && stage_elem(m.fa, fld<ESZ>(A, (int64_t)(i0 + r) * lda + 2 * g + t), S, E, G)) aSpec[r] = 1;
-        }
-      } else {
-        if (i0 + r < M && q < kc && stage_elem(m.fa, fld<ESZ>(A, (int64_t)(i0 + r) * lda + k0 + q), S, E, G))
-          aSpec[r] = 1;
-      }
-      aS[q * kFS + r] = S; aE[q * kFS + r] = E; aG[q * kFS + r] = G;
-      S = 0; E = kZeroE; G = 1;
-      if (j0 + r < N && q < kc && stage_elem(m.fb, fld<ESZ>(Bt, (int64_t)(j0 + r) * ldb + k0 + q), S, E, G))
-        bSpec[r] = 1;
-      bS[q * kFS + r] = S << m.P0; bE[q * kFS + r] = E; bG[q * kFS + r] = G;
-    }
+    stage_chunk<ESZ, SPARSE>(m, m.P0, i0, j0, k0, kc, KC, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, bS, bE, bG,
+                             aSpec, bSpec);
     __syncthreads();
     uint32_t rowsp = 0, colsp = 0;
 #pragma unroll

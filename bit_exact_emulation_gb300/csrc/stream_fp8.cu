@@ -186,11 +186,6 @@ __device__ __forceinline__ int64_t mad_wide(int32_t a, int32_t b, int64_t c) {
   asm("mad.wide.s32 %0, %1, %2, %3;" : "=l"(r) : "r"(a), "r"(b), "l"(c));
   return r;
 }
-__device__ __forceinline__ uint32_t shl_clamp(uint32_t x, uint32_t s) {   // 0 once s >= 32
-  uint32_t r;
-  asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(s));
-  return r;
-}
 
 template <int ID, int K>
 __device__ __forceinline__ uint32_t f8_exact(const DevModel &m, const uint32_t (&e)[K], const uint32_t (&sg)[K],

@@ -65,6 +65,9 @@ GEMM_CASES = [  # model, tile K (instruction inner size), input format
     (block_models("bf16", 4)["ga_rne"], 8, "bf16"),
     (block_models("bf16", 4)["ieee_exact"], 8, "bf16"),
     (dict(fmt_a="int8", fmt_b="int8", arch="exact", n_fma=16), 16, "int8"),
+    (PRESETS["cdna1_fp16"], 16, "fp16"),                # exact, N_FMA 4, with specials
+    (block_models("xf32", 2)["ieee_exact"], 8, "xf32"),
+    (block_models("e4m3", 8)["ieee_exact"], 32, "e4m3"),
 ]
 
 
@@ -96,6 +99,31 @@ def test_tile_gemm_specials_and_zero_k(L):
     assert np.array_equal(D0, C)
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "fp16"])
+def test_exact_gemm_cancellation(L, fmt):
+    """C is minus the fp32-rounded exact A*B, moved by a few units in the last place:
+    every chain ends in heavy cancellation, which the exact kernel's window must either
+    round correctly or hand to the general evaluator."""
+    M, N, K = 48, 40, 64
+    rng = np.random.default_rng(9)
+    if fmt == "bf16":
+        A, Bt, _ = W.gen_dense_bf16(M, N, K, seed=9)
+        fa = (A.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        fb = (Bt.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    else:
+        A = rng.standard_normal((M, K)).astype(np.float16).view(np.uint16)
+        Bt = rng.standard_normal((N, K)).astype(np.float16).view(np.uint16)
+        fa, fb = A.view(np.float16).astype(np.float64), Bt.view(np.float16).astype(np.float64)
+    C = (-(fa @ fb.T)).astype(np.float32).view(np.int32) + rng.integers(-2, 3, (M, N)).astype(np.int32)
+    C = C.view(np.uint32)
+    spec = block_models(fmt, 4)["ieee_exact"]
+    m = L.Model(spec)
+    D = host_u32(L.tile_gemm(m, L.tile(0, 32, 32, 8, 4), dev(A), dev(Bt), dev(C)))
+    ii, jj = all_entries(M, N)
+    want = oracle.gemm_entries(spec, K, 8, A, Bt, C, ii, jj).reshape(M, N)
+    assert np.array_equal(D, want), f"{int((D != want).sum())} mismatches"
+
+
 def test_dense_bf16_2048_sampled(L):
     """The dense BF16 GEMM workload: M = N = K = 2048, 32x32x8 bf16 tile semantics."""
     M = N = K = 2048
@@ -103,7 +131,7 @@ def test_dense_bf16_2048_sampled(L):
     rng = np.random.default_rng(11)
     ii = rng.integers(0, M, 192).astype(np.int32)
     jj = rng.integers(0, N, 192).astype(np.int32)
-    for spec in (PRESETS["cdna3_bf16"], block_models("bf16", 4)["ga_trunc"]):
+    for spec in (PRESETS["cdna3_bf16"], block_models("bf16", 4)["ga_trunc"], block_models("bf16", 4)["ieee_exact"]):
         m = L.Model(spec)
         D = host_u32(L.tile_gemm(m, L.tile(0, 32, 32, 8, 4), dev(A), dev(Bt), dev(C)))
         want = oracle.gemm_entries(spec, K, 8, A, Bt, C, ii, jj)
