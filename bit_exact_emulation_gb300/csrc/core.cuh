@@ -195,18 +195,9 @@ __device__ __forceinline__ bool hw_scale(float x, int32_t k, int rne, uint32_t &
 __device__ __forceinline__ bool hw_round32(int32_t S, int32_t k, int rne, uint32_t &bits) {
   return hw_scale(rne ? __int2float_rn(S) : __int2float_rz(S), k, rne, bits);
 }
-// 64-bit S: the magnitude is cut to its top 31 bits with the dropped bits folded into
-// bit 0 as a sticky bit (seven places below the rounding point, so RNE and RZ of the
-// cut value equal those of S), then converted with one 32-bit conversion.
 __device__ __forceinline__ bool hw_round64(int64_t S, int32_t k, int rne, uint32_t &bits) {
-  const bool neg = S < 0;
-  const uint64_t M = neg ? 0ull - (uint64_t)S : (uint64_t)S;
-  const int32_t sh = max(33 - __clzll((long long)M), 0);        // bits above the top 31
-  const uint32_t Mt = (uint32_t)(M >> sh) | ((M & ((1ull << sh) - 1ull)) != 0ull ? 1u : 0u);
-  const float x = rne ? __uint2float_rn(Mt) : __uint2float_rz(Mt);
-  return hw_scale(neg ? -x : x, k + sh, rne, bits);
+  return hw_scale(rne ? __ll2float_rn(S) : __ll2float_rz(S), k, rne, bits);
 }
-
 // ---------------------------------------------------------------------------
 // terms of eq. (1)
 // ---------------------------------------------------------------------------
