@@ -249,6 +249,28 @@ def test_empty_single_and_ragged(L):
         assert np.array_equal(got, oracle.block_fma(spec, a, b, c))
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_entry_point(L, pinned):
+    """mcemu_block_fma_host on page-locked buffers (read in place by the kernel) and on
+    pageable ones (staged through the workspace), against the device entry point."""
+    n = 3 * 4_194_304 // 2 + 7                    # crosses the staging chunk size
+    for fmt, k in (("bf16", 4), ("e4m3", 8)):
+        a, b, c = W.gen_block_fma_set(fmt, n, k, seed=23)
+        m = L.Model(block_models(fmt, k)["ga_rne"])
+        want = gpu_block(L, block_models(fmt, k)["ga_rne"], a, b, c)
+
+        def host(x):
+            x = np.ascontiguousarray(x)
+            t = torch.from_numpy(x.view({np.uint16: np.int16, np.uint32: np.int32}.get(x.dtype.type, x.dtype)))
+            return t.pin_memory() if pinned else t
+        ha, hb, hc = host(a), host(b), host(c)
+        hd = torch.empty(n, dtype=torch.int32)
+        hd = hd.pin_memory() if pinned else hd
+        ws = torch.empty(L.block_fma_host_workspace(m), dtype=torch.uint8, device="cuda")
+        L.block_fma_host(m, ha, hb, hc, hd, ws)
+        assert np.array_equal(hd.numpy().view(np.uint32), want)
+
+
 def test_misaligned_pointer_is_rejected(L):
     spec = block_models("fp16", 4)["ga_rne"]
     m = L.Model(spec)
