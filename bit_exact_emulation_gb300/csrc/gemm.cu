@@ -115,6 +115,14 @@ __global__ void __launch_bounds__(kT *kT) sparse_generic_kernel(
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
+// do the M x N u32 matrices at C (ldc) and D (ldd) share any bytes?
+static bool overlaps(const uint32_t *C, int64_t ldc, const uint32_t *D, int64_t ldd, int M, int N) {
+  if (M <= 0 || N <= 0) return false;
+  const uintptr_t c0 = (uintptr_t)C, c1 = (uintptr_t)(C + (int64_t)(M - 1) * ldc + N);
+  const uintptr_t d0 = (uintptr_t)D, d1 = (uintptr_t)(D + (int64_t)(M - 1) * ldd + N);
+  return c0 < d1 && d0 < c1;
+}
+
 static int elem_size(const DevModel &m) { return m.fa.is_int ? 1 : (int)(m.fa.sshift + 1) / 8; }
 
 template <class Kern>
@@ -129,8 +137,12 @@ int launch_tile_gemm(const DevModel &m, int kt, int M, int N, int K, const void 
                      int64_t ldd, void *stream) {
   cudaStream_t s = (cudaStream_t)stream;
   if (kt > 1024) return MCEMU_ERR_UNSUPPORTED;
-  if (gemm_fast_ok(m) && kt <= 64) return launch_tile_gemm_fast(m, kt, M, N, K, A, lda, Bt, ldb, C, ldc, D, ldd, stream);
-  if (gemm_exact_ok(m) && kt <= 64)
+  // the fast kernels leave some outputs to a second pass that reads C again, so an
+  // in-place accumulation (C overlapping D) takes the general kernel
+  const bool alias = C && overlaps(C, ldc, D, ldd, M, N);
+  if (!alias && gemm_fast_ok(m) && kt <= 64)
+    return launch_tile_gemm_fast(m, kt, M, N, K, A, lda, Bt, ldb, C, ldc, D, ldd, stream);
+  if (!alias && gemm_exact_ok(m) && kt <= 64)
     return launch_tile_gemm_exact(m, kt, M, N, K, A, lda, Bt, ldb, C, ldc, D, ldd, stream);
   const size_t shm = (size_t)2 * kT * chunk_len(kt) * 4;
   dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT), block(kT, kT);
@@ -158,9 +170,10 @@ int launch_sparse24_gemm(const DevModel &m, int kt, int M, int N, int K, const v
                          const uint32_t *C, int64_t ldc, uint32_t *D, int64_t ldd, void *stream) {
   cudaStream_t s = (cudaStream_t)stream;
   if (kt > 1024) return MCEMU_ERR_UNSUPPORTED;
-  if (sparse_fast_ok(m, kt))
+  const bool alias = C && overlaps(C, ldc, D, ldd, M, N);
+  if (!alias && sparse_fast_ok(m, kt))
     return launch_sparse24_gemm_fast(m, kt, M, N, K, Ac, ldac, meta, ldm, Bt, ldb, C, ldc, D, ldd, stream);
-  if (gemm_exact_ok(m) && m.k % 2 == 0 && 2 * m.k <= 32 && kt <= 64 && elem_size(m) <= 2)
+  if (!alias && gemm_exact_ok(m) && m.k % 2 == 0 && 2 * m.k <= 32 && kt <= 64 && elem_size(m) <= 2)
     return launch_sparse24_gemm_exact(m, kt, M, N, K, Ac, ldac, meta, ldm, Bt, ldb, C, ldc, D, ldd, stream);
   const int Kc = K / 2, ktc = kt / 2;
   const size_t shm = (size_t)4 * kT * chunk_len(ktc) * 4;

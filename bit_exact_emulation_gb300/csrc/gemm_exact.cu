@@ -10,8 +10,8 @@
 // lies in [W, W + terms) units; when |W| >= 2^26 the rounding boundaries of that
 // range are multiples of 4 units and the rounding of 4W and 4(W + terms) - 1 (units
 // of 2^(L-2)) brackets it: equal results are the correctly rounded sum.  Anything else
-// (a special value, heavy cancellation, a subnormal result) sends the output's whole
-// chain to the general evaluator, as in the global-alignment kernel.
+// (a special value, heavy cancellation, a subnormal result) marks the output, and the
+// fixup pass evaluates its whole chain with the general evaluator.
 #include "gemm_fast.cuh"
 
 namespace mcemu {
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kFThreads, 1) gemm_exact_kernel(const __grid_c
         int64_t W[kFT][kFT];
         int32_t C1[kFT][kFT];
         uint32_t st[kFT][kFT];                               // nonzero once a term lost bits
+        uint32_t nzm = 0;                                    // outputs with a nonzero product or c
 #pragma unroll
         for (int a = 0; a < kFT; a++)
 #pragma unroll
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(kFThreads, 1) gemm_exact_kernel(const __grid_c
             uint32_t cS, cneg;
             int32_t cE;
             decode_c(m, acc[a][b], cS, cE, cneg);
+            if (T[a][b] > -1024 || cS) nzm |= 1u << (a * kFT + b);
             int32_t top = T[a][b] + 2;                       // products: |p| < 2^(E_a + E_b + 2)
             if (cS) top = max(top, cE + 1);
             const int32_t L = top - 61 + logk;
@@ -137,8 +139,10 @@ __global__ void __launch_bounds__(kFThreads, 1) gemm_exact_kernel(const __grid_c
             uint32_t lo = 0, hi = 1;
             bool ok = !((((rowsp >> a) | (colsp >> b)) & 1u) || (acc[a][b] & 0x7F800000u) == 0x7F800000u) &&
                       L > kNegE / 2;
-            if (st[a][b] == 0u)                              // the window holds the exact sum
-              ok = ok && w != 0 && hw_round64(w, L, m.rne, lo);
+            if (st[a][b] == 0u && w == 0)                    // exact zero: +0 unless every term is zero
+              ok = ok && ((nzm >> (a * kFT + b)) & 1u);
+            else if (st[a][b] == 0u)                         // the window holds the exact sum
+              ok = ok && hw_round64(w, L, m.rne, lo);
             else
               ok = ok && (w >= (1ll << 26) || w <= -(1ll << 26)) && hw_round64(4 * w, L - 2, m.rne, lo) &&
                    hw_round64(4 * (w + nt + 1) - 1, L - 2, m.rne, hi) && lo == hi;
@@ -148,23 +152,14 @@ __global__ void __launch_bounds__(kFThreads, 1) gemm_exact_kernel(const __grid_c
       }
     }
   }
+  // flagged outputs get the mark; gemm_fixup_kernel recomputes them afterwards
 #pragma unroll
   for (int a = 0; a < kFT; a++)
 #pragma unroll
     for (int b = 0; b < kFT; b++) {
       const int i = i0 + ti + a, j = j0 + tj + b;
-      if (i < M && j < N && !((redo >> (a * kFT + b)) & 1u)) D[(int64_t)i * ldd + j] = acc[a][b];
+      if (i < M && j < N) D[(int64_t)i * ldd + j] = ((redo >> (a * kFT + b)) & 1u) ? redo_mark(m) : acc[a][b];
     }
-  while (redo) {
-    const int o = __ffs(redo) - 1;
-    redo &= redo - 1;
-    const int i = i0 + ti + o / kFT, j = j0 + tj + o % kFT;
-    if (i >= M || j >= N) continue;
-    uint32_t r;
-    if constexpr (SPARSE) r = chain_sparse_generic<ESZ>(m, kt / 2, K / 2, A, lda, meta, ldm, Bt, ldb, i, j, C, ldc);
-    else r = chain_generic<ESZ>(m, kt, K, A, lda, Bt, ldb, i, j, C, ldc);
-    D[(int64_t)i * ldd + j] = r;
-  }
 }
 
 // true when the exact kernel implements the model (float operands of at most 11
@@ -188,7 +183,8 @@ static int run_exact(const DevModel &m, int kt, int kblk, int M, int N, int K, c
   dim3 grid((N + kFB - 1) / kFB, (M + kFB - 1) / kFB);
   kern<<<grid, kFThreads, shm, s>>>(m, kt, kblk, logk, M, N, K, (const uint8_t *)A, lda, meta, ldm,
                                     (const uint8_t *)Bt, ldb, C, ldc, D, ldd);
-  return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return MCEMU_ERR_CUDA;
+  return run_fixup<ESZ, SPARSE>(m, kt, M, N, K, A, lda, meta, ldm, Bt, ldb, C, ldc, D, ldd, s);
 }
 
 int launch_tile_gemm_exact(const DevModel &m, int kt, int M, int N, int K, const void *A, int64_t lda,

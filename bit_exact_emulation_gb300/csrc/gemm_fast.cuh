@@ -132,20 +132,26 @@ __device__ __noinline__ uint32_t chain_sparse_generic(const DevModel &m, int ktc
   return acc;
 }
 
-// Early-c merge of one output: S = S_p + aligned c, rounded in hardware.  False when
-// the sum is zero (its sign needs the inputs) or the result is subnormal.
-__device__ __forceinline__ bool merge_early(const DevModel &m, int32_t Sp, int32_t emax, uint32_t cb, uint32_t &r) {
+// Early-c merge of one output: S = S_p + aligned c, rounded in hardware.  A zero sum
+// is +0 when some product or c is nonzero; false for a zero sum of zero terms (its
+// sign needs the inputs) or a subnormal result.
+__device__ __forceinline__ bool merge_early(const DevModel &m, int32_t Sp, int32_t emax, uint32_t cb, bool have_p,
+                                            uint32_t &r) {
   uint32_t cS, cneg;
   int32_t cE;
   decode_c(m, cb, cS, cE, cneg);
   int32_t S = Sp;
   if (cS) S += align_term<uint32_t, int32_t>(cS << m.P0c, cneg, emax + m.R0c - cE, 0);
-  if (S == 0) return false;
+  if (S == 0) {
+    r = 0u;
+    return have_p || cS != 0u;
+  }
   return hw_round32(S, emax - m.F, m.rne, r);
 }
 
-// Algorithm 1, lines 5-15, for one output with hardware rounding.  False for a zero
-// or subnormal result (the general evaluator then decides).
+// Algorithm 1, lines 5-15, for one output with hardware rounding.  A zero sum is +0
+// when some product or c is nonzero; false for a zero sum of zero terms or a
+// subnormal result (the general evaluator then decides).
 __device__ __forceinline__ bool merge_late(const DevModel &m, int32_t Sp, int32_t emax, uint32_t cb, uint32_t &r) {
   uint32_t cS, cneg;
   int32_t cE;
@@ -162,7 +168,10 @@ __device__ __forceinline__ bool merge_late(const DevModel &m, int32_t Sp, int32_
       sc = sh >= 0 ? sar32(v, sh) : v * (1 << (-sh));
     }
     const int32_t Sacc = Sp + sc;                       // line 8
-    if (Sacc == 0) return false;
+    if (Sacc == 0) {                                     // a nonzero product cancelled: +0
+      r = 0u;
+      return true;
+    }
     return hw_round32(Sacc, emax - m.F, m.rne, r);      // line 15
   }
   int64_t Sp2 = 0;                                       // line 10
@@ -172,7 +181,10 @@ __device__ __forceinline__ bool merge_late(const DevModel &m, int32_t Sp, int32_
   }
   const int64_t vc = cneg ? -(int64_t)cS : (int64_t)cS;
   const int64_t Sacc = Sp2 + vc * ((int64_t)1 << (m.psum_frac - 23));   // line 11
-  if (Sacc == 0) return false;
+  if (Sacc == 0) {
+    r = 0u;
+    return have_p || cS != 0u;
+  }
   const bool neg = Sacc < 0;
   uint64_t M = neg ? (uint64_t)(-Sacc) : (uint64_t)Sacc;
   int32_t lsb = ec - m.psum_frac;
@@ -184,6 +196,12 @@ __device__ __forceinline__ bool merge_late(const DevModel &m, int32_t Sp, int32_
     lsb += rsh;
   }
   return hw_round64(neg ? -(int64_t)M : (int64_t)M, lsb, m.rne, r);   // line 15
+}
+
+// A NaN pattern no model returns (their NaN results are always nan_bits): it marks
+// an output the fast kernel left to the general evaluator.
+__host__ __device__ __forceinline__ uint32_t redo_mark(const DevModel &m) {
+  return m.nan_bits == 0x7FFFFFFFu ? 0xFFFFFFFFu : 0x7FFFFFFFu;
 }
 
 template <int OUT>
@@ -269,6 +287,7 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
 #pragma unroll
             for (int b = 0; b < kFT; b++) emax[a][b] = __viaddmax_s32(xa[a], xb[b], emax[a][b]);
         }
+        uint32_t hpm = 0;
         // ---- c's exponent (early c) and the shift base
         int32_t base[kFT][kFT];
         int32_t Sp[kFT][kFT];
@@ -283,6 +302,7 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
               const bool cz = (ef == 0u) && ((mf & m.c_sub_keep) == 0u);
               const int32_t ec = cz ? m.c_zero_exp : (int32_t)max(ef, 1u) - 127;
               em = max(max(em, ec), m.emin_lim);
+              if (emax[a][b] > -1024) hpm |= 1u << (a * kFT + b);   // some product is nonzero
               emax[a][b] = em;
             }
             base[a][b] = em + m.R0;
@@ -318,7 +338,8 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
             bool ok = !((((rowsp >> a) | (colsp >> b)) & 1u) || (cb & 0x7F800000u) == 0x7F800000u ||
                         (m.prod_ovf && emax[a][b] >= 126));
             if (ok) {
-              if constexpr (ARCH == MCEMU_ARCH_GA_EARLY) ok = merge_early(m, Sp[a][b], emax[a][b], cb, r);
+              if constexpr (ARCH == MCEMU_ARCH_GA_EARLY)
+                ok = merge_early(m, Sp[a][b], emax[a][b], cb, (hpm >> (a * kFT + b)) & 1u, r);
               else ok = merge_late(m, Sp[a][b], emax[a][b], cb, r);
             }
             if (!ok) redo |= 1u << (a * kFT + b);
@@ -326,6 +347,19 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
           }
       }
     }
+  }
+  if constexpr (OUT == 0) {
+    // flagged outputs get the mark; gemm_fixup_kernel recomputes them afterwards
+    // (C does not alias D on this path).  Keeping the general evaluator out of this
+    // kernel keeps its register allocation free of a call.
+#pragma unroll
+    for (int a = 0; a < kFT; a++)
+#pragma unroll
+      for (int b = 0; b < kFT; b++) {
+        const int i = i0 + ti + a, j = j0 + tj + b;
+        if (i < M && j < N) D[(int64_t)i * ldd + j] = ((redo >> (a * kFT + b)) & 1u) ? redo_mark(m) : acc[a][b];
+      }
+    return;
   }
   // outputs on the fast path
 #pragma unroll
@@ -335,8 +369,7 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
       const int i = i0 + ti + a, j = j0 + tj + b;
       if (i < M && j < N && !((redo >> (a * kFT + b)) & 1u)) store_out<OUT>(D, D64, first, ldd, i, j, acc[a][b]);
     }
-  // rare: the whole chain of each flagged output with the general evaluator (c is
-  // read before this thread writes the output, so C may alias D)
+  // rare: the whole chain of each flagged output with the general evaluator
   while (redo) {
     const int o = __ffs(redo) - 1;
     redo &= redo - 1;
@@ -347,6 +380,33 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
     else r = chain_generic<ESZ>(m, kt, K, A, lda, Bt, ldb, i, j, C, ldc);
     store_out<OUT>(D, D64, first, ldd, i, j, r);
   }
+}
+
+// Whole chains of the outputs a fast kernel marked, one output per thread.
+template <int ESZ, int SPARSE>
+__global__ void __launch_bounds__(256) gemm_fixup_kernel(const __grid_constant__ DevModel m, int kt, int M, int N,
+                                                         int K, const uint8_t *__restrict__ A, int64_t lda,
+                                                         const uint8_t *__restrict__ meta, int64_t ldm,
+                                                         const uint8_t *__restrict__ Bt, int64_t ldb,
+                                                         const uint32_t *C, int64_t ldc, uint32_t *D, int64_t ldd) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (int64_t)M * N) return;
+  const int i = (int)(t / N), j = (int)(t % N);
+  if (D[(int64_t)i * ldd + j] != redo_mark(m)) return;
+  uint32_t r;
+  if constexpr (SPARSE) r = chain_sparse_generic<ESZ>(m, kt / 2, K / 2, A, lda, meta, ldm, Bt, ldb, i, j, C, ldc);
+  else r = chain_generic<ESZ>(m, kt, K, A, lda, Bt, ldb, i, j, C, ldc);
+  D[(int64_t)i * ldd + j] = r;
+}
+
+template <int ESZ, int SPARSE>
+static int run_fixup(const DevModel &m, int kt, int M, int N, int K, const void *A, int64_t lda,
+                     const uint8_t *meta, int64_t ldm, const void *Bt, int64_t ldb, const uint32_t *C, int64_t ldc,
+                     uint32_t *D, int64_t ldd, cudaStream_t s) {
+  const int64_t total = (int64_t)M * N;
+  gemm_fixup_kernel<ESZ, SPARSE><<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+      m, kt, M, N, K, (const uint8_t *)A, lda, meta, ldm, (const uint8_t *)Bt, ldb, C, ldc, D, ldd);
+  return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
 }
 
 template <int ARCH, int ESZ, int OUT = 0, int SPARSE = 0>
@@ -362,7 +422,9 @@ static int run_fast(const DevModel &m, int kt, int M, int N, int K, const void *
   const int kblk = SPARSE ? 2 * m.k : m.k;
   kern<<<grid, kFThreads, shm, s>>>(m, kt, kblk, M, N, K, (const uint8_t *)A, lda, meta, ldm, (const uint8_t *)Bt,
                                     ldb, C, ldc, D, D64, first, ldd);
-  return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return MCEMU_ERR_CUDA;
+  if constexpr (OUT == 0) return run_fixup<ESZ, SPARSE>(m, kt, M, N, K, A, lda, meta, ldm, Bt, ldb, C, ldc, D, ldd, s);
+  return MCEMU_OK;
 }
 
 }  // namespace mcemu

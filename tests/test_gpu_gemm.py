@@ -124,6 +124,23 @@ def test_exact_gemm_cancellation(L, fmt):
     assert np.array_equal(D, want), f"{int((D != want).sum())} mismatches"
 
 
+@pytest.mark.parametrize("name", ["cdna3_bf16", "ga_rne", "ieee_exact"])
+def test_in_place_accumulation(L, name):
+    """D = A*B + D with D the same buffer as C (the general kernel then runs), and D a
+    separate buffer (the fast kernels), against the oracle."""
+    spec = PRESETS["cdna3_bf16"] if name == "cdna3_bf16" else block_models("bf16", 4)[name]
+    M, N, K = 70, 66, 96
+    A, Bt, C = operands("bf16", M, N, K, seed=12)
+    m = L.Model(spec)
+    ii, jj = all_entries(M, N)
+    want = oracle.gemm_entries(spec, K, 8, A, Bt, C, ii, jj).reshape(M, N)
+    dC = dev(C)
+    D_sep = host_u32(L.tile_gemm(m, L.tile(0, 32, 32, 8, 4), dev(A), dev(Bt), dC))
+    L.tile_gemm(m, L.tile(0, 32, 32, 8, 4), dev(A), dev(Bt), dC, dC)
+    assert np.array_equal(D_sep, want)
+    assert np.array_equal(host_u32(dC), want)
+
+
 def test_dense_bf16_2048_sampled(L):
     """The dense BF16 GEMM workload: M = N = K = 2048, 32x32x8 bf16 tile semantics."""
     M = N = K = 2048
