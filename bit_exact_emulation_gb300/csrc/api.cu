@@ -559,7 +559,8 @@ extern "C" size_t mcemu_multiword_workspace(int n_words, int M, int N, int K) {
   if (n_words < 1 || n_words > 8 || M < 0 || N < 0 || K < 0) return 0;
   size_t wa = ((size_t)n_words * M * K * 2 + 255) & ~(size_t)255;
   size_t wb = ((size_t)n_words * N * K * 2 + 255) & ~(size_t)255;
-  return wa + wb;
+  size_t wp = ((size_t)M * N * 4 + 255) & ~(size_t)255;       // one fp32 word product
+  return wa + wb + wp;
 }
 
 extern "C" int mcemu_multiword_gemm(mcemu_model_t word_model, const mcemu_tile_desc *tile, int n_words,

@@ -72,8 +72,6 @@ bool gemm_fast_ok(const DevModel &m);
 int launch_tile_gemm_fast(const DevModel &m, int kt, int M, int N, int K, const void *A, int64_t lda,
                           const void *Bt, int64_t ldb, const uint32_t *C, int64_t ldc, uint32_t *D, int64_t ldd,
                           void *stream);
-int launch_tile_gemm_fast_acc64(const DevModel &m, int kt, int M, int N, int K, const uint16_t *Aw, int64_t lda,
-                                const uint16_t *Bw, int64_t ldb, double *D, int64_t ldd, int first, void *stream);
 bool sparse_fast_ok(const DevModel &m, int kt);
 bool gemm_exact_ok(const DevModel &m);
 int launch_tile_gemm_exact(const DevModel &m, int kt, int M, int N, int K, const void *A, int64_t lda,

@@ -128,6 +128,16 @@ __global__ void __launch_bounds__(kMwTile *kMwTile) multiword_kernel(
   D[(int64_t)i * ldd + j] = d;
 }
 
+// D = fl64(D + P) (or fl64(0 + P) for the first word product), P the fp32 bits of one
+// word product
+__global__ void __launch_bounds__(256) combine_kernel(int M, int N, const uint32_t *__restrict__ P, double *D,
+                                                      int64_t ldd, int first) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (int64_t)M * N) return;
+  double *p = D + (t / N) * ldd + t % N;
+  *p = __dadd_rn(first ? 0.0 : *p, (double)__uint_as_float(P[t]));
+}
+
 template <int NW>
 static int run_mw(const DevModel &m, int kt, int truncated, int M, int N, int K, const uint16_t *Aw,
                   const uint16_t *Bw, double *D, int64_t ldd, cudaStream_t s) {
@@ -158,16 +168,21 @@ int launch_multiword_gemm(const DevModel &m, int kt, int n_words, int truncated,
     if (st != MCEMU_OK) return st;
   }
   if (gemm_fast_ok(m) && kt <= 64) {
-    // one fast tile GEMM per word pair, each adding its fp32 result into the binary64 D
-    // in the combine order: i + j descending, then i ascending
+    // one fast tile GEMM per word pair into the fp32 buffer after the words, each
+    // added into the binary64 D in the combine order: i + j descending, then i ascending
+    const size_t wb = ((size_t)n_words * N * K * 2 + 255) & ~(size_t)255;
+    uint32_t *P = (uint32_t *)((uint8_t *)ws + wa + wb);
     int first = 1;
     for (int sum = 2 * n_words; sum >= 2; sum--)
       for (int wi = 1; wi <= n_words; wi++) {
         const int wj = sum - wi;
         if (wj < 1 || wj > n_words || (truncated && wi + wj > n_words + 1)) continue;
-        const int st = launch_tile_gemm_fast_acc64(m, kt, M, N, K, Aw + (size_t)(wi - 1) * M * K, K,
-                                                   Bw + (size_t)(wj - 1) * N * K, K, D, ldd, first, stream);
+        int st = launch_tile_gemm_fast(m, kt, M, N, K, Aw + (size_t)(wi - 1) * M * K, K,
+                                       Bw + (size_t)(wj - 1) * N * K, K, nullptr, 0, P, N, stream);
         if (st != MCEMU_OK) return st;
+        const int64_t total = (int64_t)M * N;
+        combine_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(M, N, P, D, ldd, first);
+        if (cudaGetLastError() != cudaSuccess) return MCEMU_ERR_CUDA;
         first = 0;
       }
     return MCEMU_OK;
@@ -185,8 +200,8 @@ int launch_multiword_gemm(const DevModel &m, int kt, int n_words, int truncated,
 // it (a host program that only holds buffers handed to it, a loop whose device
 // memory is budgeted up front): the words of A and B go to a fixed array of this
 // module's device memory instead of caller workspace.  The split kernel writes
-// every word the GEMM kernel reads, so nothing in the array has to start at
-// zero.  One array per device serves every call: calls whose kernels may
+// every word the GEMM kernel reads, and each word product is written before the
+// combine reads it, so nothing in the array has to start at zero.  One array per device serves every call: calls whose kernels may
 // overlap race on it.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) uint8_t g_mw_static_ws[MCEMU_MULTIWORD_STATIC_BYTES];

@@ -236,7 +236,8 @@ int mcemu_multiword_split(int n_words, size_t n, const double *x, uint16_t *word
  * All n_words^2 pairs, or with MCEMU_WORDS_TRUNCATED those with
  * i + j <= n_words + 1.  The binary64 sum runs over i+j descending, then i
  * ascending.  A [M][K] (lda), Bt [N][K] (ldb) binary64; D [M][N] binary64.
- * workspace: device, >= mcemu_multiword_workspace(n_words, M, N, K). */
+ * workspace: device, >= mcemu_multiword_workspace(n_words, M, N, K) bytes: the
+ * BF16 words of A and B and one fp32 word product. */
 int mcemu_multiword_gemm(mcemu_model_t word_model, const mcemu_tile_desc *tile, int n_words,
                          int product_set, int M, int N, int K, const double *A, int64_t lda,
                          const double *Bt, int64_t ldb, double *D, int64_t ldd,
@@ -245,9 +246,9 @@ size_t mcemu_multiword_workspace(int n_words, int M, int N, int K);
 /* ---- multi-word GEMM with no allocation (library addition) ----------------
  * The paper has no counterpart to this call: it is a convenience of this
  * library.  It computes exactly what mcemu_multiword_gemm computes (same
- * kernels, same results bit for bit), but takes no workspace argument: the
- * BF16 words of A and B are written to a fixed array in the library's own
- * device memory, MCEMU_MULTIWORD_STATIC_BYTES long.  It is meant for callers
+ * kernels, same results bit for bit), but takes no workspace argument: its
+ * workspace (the BF16 words of A and B and one fp32 word product) is a fixed
+ * array in the library's own device memory, MCEMU_MULTIWORD_STATIC_BYTES long.  It is meant for callers
  * that cannot allocate device memory where they call it: a host program that
  * only holds device buffers handed to it, or a loop whose device memory was
  * budgeted up front and must not grow.  The call itself allocates nothing.
@@ -255,8 +256,8 @@ size_t mcemu_multiword_workspace(int n_words, int M, int N, int K);
  * the array's device address once; make that first call before any stream
  * capture.  Limit: mcemu_multiword_workspace(n_words, M, N, K) must not exceed
  * MCEMU_MULTIWORD_STATIC_BYTES, else MCEMU_ERR_WORKSPACE and nothing runs.
- * Nothing in the array has to start at zero (every word is written before it
- * is read).  The array is shared by all calls on a device: two calls whose
+ * Nothing in the array has to start at zero (everything in it is written
+ * before it is read).  The array is shared by all calls on a device: two calls whose
  * kernels may overlap (other streams, other host threads) race on it; order
  * them on one stream.  Other arguments and errors as mcemu_multiword_gemm;
  * MCEMU_ERR_CUDA when the address look-up fails. */

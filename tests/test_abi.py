@@ -116,7 +116,7 @@ def test_null_arguments_are_rejected(L):
     assert lib.mcemu_sparse24_compress(4, 0, 4, 6, None, 6, None, 3, None, 1, None, None) == 1   # K % 4
     assert lib.mcemu_multiword_gemm(m.handle, ctypes.byref(t), 3, 0, 4, 4, 4, None, 4, None, 4, None, 4,
                                     None, 0, None) == 2                                       # fp16 words
-    assert lib.mcemu_multiword_workspace(3, 4096, 4096, 4096) == 3 * 2 * 4096 * 4096 * 2
+    assert lib.mcemu_multiword_workspace(3, 4096, 4096, 4096) == 3 * 2 * 4096 * 4096 * 2 + 4096 * 4096 * 4
 
 
 def test_tile_info_matches_oracle(L):
