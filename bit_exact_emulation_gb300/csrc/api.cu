@@ -276,6 +276,8 @@ static DevModel derive(const mcemu_model_desc *d) {
   double cmax = (double)((1ll << 24) - 1) * (double)(1ll << (m.P0c < 40 ? m.P0c : 40));
   double bound = (double)m.k * pmax + cmax;
   m.wide = (m.F + 2 > 31) || (m.mab > 22) || bound >= 2147483648.0;
+  m.p0mul = m.P0 < 32 ? 1u << m.P0 : 0u;
+  m.p0cmul = m.P0c < 32 ? 1u << m.P0c : 0u;
   return m;
 }
 

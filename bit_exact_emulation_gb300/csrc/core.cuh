@@ -297,10 +297,22 @@ __device__ __forceinline__ uint32_t arch_ga_early(const DevModel &m, const Term<
   emax = max(emax, ec);
   AT S = 0;
   const int32_t base = emax + m.R0;
+  if (sizeof(AT) == 4 && !m.align_rd) {
+    // truncation with 32-bit sums: the pre-shift and the sign as multiplies (FMA pipe),
+    // one funnel shift per term on the ALU pipe
 #pragma unroll
-  for (int l = 0; l < K; l++)
-    if (l < nt) S += align_term<UT, AT>(p[l].U << m.P0, p[l].neg, base - p[l].e, m.align_rd);
-  if (cS) S += align_term<UT, AT>((UT)cS << m.P0c, cneg, emax + m.R0c - cE, m.align_rd);
+    for (int l = 0; l < K; l++)
+      if (l < nt) {
+        const uint32_t t = shr32((uint32_t)p[l].U * m.p0mul, base - p[l].e);
+        S += (AT)((int32_t)t * (1 - 2 * (int32_t)p[l].neg));
+      }
+    if (cS) S += (AT)((int32_t)shr32(cS * m.p0cmul, emax + m.R0c - cE) * (1 - 2 * (int32_t)cneg));
+  } else {
+#pragma unroll
+    for (int l = 0; l < K; l++)
+      if (l < nt) S += align_term<UT, AT>(p[l].U << m.P0, p[l].neg, base - p[l].e, m.align_rd);
+    if (cS) S += align_term<UT, AT>((UT)cS << m.P0c, cneg, emax + m.R0c - cE, m.align_rd);
+  }
   if (S == 0) return zero_result<K, UT>(p, nt, cS, cneg);
   return pack_sum<AT>(S, emax - m.F, m);
 }

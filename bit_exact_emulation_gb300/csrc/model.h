@@ -52,6 +52,7 @@ struct DevModel {
   int32_t P0c, R0c;       // the same for c (F - 23)
   int32_t bias_sum;       // bias_a + bias_b (products carry biased exponents)
   int32_t wide;           // 1 when sums need 64-bit integers
+  uint32_t p0mul, p0cmul; // 2^P0 and 2^P0c (32-bit sums): the pre-shifts as multiplies
 };
 
 struct Model {
