@@ -576,11 +576,11 @@ __device__ __forceinline__ uint32_t arch_exact(const DevModel &m, const Term<UT>
 // constant Q = 62 - wid and r = Q - lsb + L >= 0: one arithmetic shift floors it
 // into the window and the bits it drops set the sticky count nb.  The true sum then
 // lies in [W, W + nb) units, excluding W itself when nb > 0.  With |W| >= 2^26 the
-// rounding boundaries of that range are multiples of 4 units, so W + 1/4 and
-// W + nb - 1/4 (4W + 1 and 4(W + nb) - 1 in units of 2^(L-2)) round like every value
-// the sum can take next to them: when both give the same fp32 value, that value is
-// the correctly rounded sum.  Otherwise (heavy cancellation, or a subnormal result)
-// the full-width evaluator decides.
+// rounding boundaries of that range are multiples of 4 units (for subnormal results
+// too: the window then sits at least 152 places below 2^-126), so W + 1/2 and
+// W + nb - 1/2 round like every value the sum can take next to them: when both give
+// the same fp32 value, that value is the correctly rounded sum.  Otherwise (heavy
+// cancellation) the full-width evaluator decides.
 template <int K>
 struct ExactLog {
   static constexpr int v = K + 1 <= 2 ? 1 : K + 1 <= 4 ? 2 : K + 1 <= 8 ? 3 : K + 1 <= 16 ? 4 : K + 1 <= 32 ? 5 : 6;
@@ -641,10 +641,19 @@ __device__ __forceinline__ uint32_t arch_exact64(const DevModel &m, const Term<U
   uint32_t lo, hi;
   if (nb == 0) {
     if (W == 0) return zero_result<K, UT>(p, K, cS, cneg);
-    if (hw_round64(W, L, m.rne, lo) && !m.sub_out_flush) return lo;
-  } else if (!m.sub_out_flush && (W >= (1ll << 26) || W <= -(1ll << 26)) && hw_round64(4 * W + 1, L - 2, m.rne, lo) &&
-             hw_round64(4 * (W + nb) - 1, L - 2, m.rne, hi) && lo == hi) {
-    return lo;
+    if (!m.sub_out_flush && hw_round64(W, L, m.rne, lo)) return lo;
+    // subnormal or flushed result of an exact window: integer rounding
+    return round_pack(W < 0 ? 0ull - (uint64_t)W : (uint64_t)W, L, W < 0 ? 1u : 0u, false, m.rne, m.sub_out_flush);
+  }
+  if (W >= (1ll << 26) || W <= -(1ll << 26)) {
+    // the sum lies in (W, W + nb): W + 1/2 and W + nb - 1/2 (2W + 1 and 2(W + nb) - 1 in
+    // units of 2^(L-1)) round like every value next to them
+    const int64_t X = 2 * W + 1, Y = 2 * (W + nb) - 1;
+    if (!m.sub_out_flush && hw_round64(X, L - 1, m.rne, lo) && hw_round64(Y, L - 1, m.rne, hi) && lo == hi)
+      return lo;
+    lo = round_pack(X < 0 ? 0ull - (uint64_t)X : (uint64_t)X, L - 1, X < 0 ? 1u : 0u, false, m.rne, m.sub_out_flush);
+    hi = round_pack(Y < 0 ? 0ull - (uint64_t)Y : (uint64_t)Y, L - 1, Y < 0 ? 1u : 0u, false, m.rne, m.sub_out_flush);
+    if (lo == hi) return lo;
   }
   int64_t V[K + 1];
   int32_t Ls[K + 1];
