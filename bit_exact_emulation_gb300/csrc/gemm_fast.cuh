@@ -174,28 +174,27 @@ __device__ __forceinline__ bool merge_late(const DevModel &m, int32_t Sp, int32_
     }
     return hw_round32(Sacc, emax - m.F, m.rne, r);      // line 15
   }
-  int64_t Sp2 = 0;                                       // line 10
-  if (have_p) {
-    const int32_t sh = ec - emax - (m.psum_frac - m.F);
-    Sp2 = sh >= 0 ? sar64((int64_t)Sp, sh) : (int64_t)Sp * ((int64_t)1 << (-sh));
-  }
+  // line 10: S_p on c's grid with RD (floor) at psum_frac fraction bits; in this branch
+  // e_max < e_c, so the shift is at least 1 - (psum_frac - F_p) >= -8 and the product
+  // sum, pre-shifted by 16, is floored by one arithmetic shift
+  int64_t Sacc = have_p ? (((int64_t)Sp << 16) >> min(ec - emax - (m.psum_frac - m.F) + 16, 63)) : 0;
   const int64_t vc = cneg ? -(int64_t)cS : (int64_t)cS;
-  const int64_t Sacc = Sp2 + vc * ((int64_t)1 << (m.psum_frac - 23));   // line 11
+  Sacc += vc * ((int64_t)1 << (m.psum_frac - 23));       // line 11
   if (Sacc == 0) {
     r = 0u;
     return have_p || cS != 0u;
   }
-  const bool neg = Sacc < 0;
-  uint64_t M = neg ? (uint64_t)(-Sacc) : (uint64_t)Sacc;
+  // lines 12-13: normalise (exponent floored at -126) and RD to post_norm_frac bits.
+  // The leading bit of |S| is found from S xor its sign: one place lower only when
+  // |S| is a power of two, where every lower bit is zero and the RD is exact anyway.
   int32_t lsb = ec - m.psum_frac;
-  int32_t E = 63 - __clzll((long long)M) + lsb;          // line 12
-  E = max(E, -126);
-  const int32_t rsh = E - m.post_norm_frac - lsb;        // line 13
+  const int32_t p = 63 - __clzll((long long)(Sacc ^ (Sacc >> 63)));
+  const int32_t rsh = max(p + lsb, -126) - m.post_norm_frac - lsb;
   if (rsh > 0) {
-    M = neg ? ((M + ((1ull << rsh) - 1ull)) >> rsh) : (M >> rsh);
+    Sacc >>= min(rsh, 63);                               // floor = RD for either sign
     lsb += rsh;
   }
-  return hw_round64(neg ? -(int64_t)M : (int64_t)M, lsb, m.rne, r);   // line 15
+  return hw_round64(Sacc, lsb, m.rne, r);                // line 15
 }
 
 // A NaN pattern no model returns (their NaN results are always nan_bits): it marks
