@@ -132,19 +132,13 @@ __device__ __noinline__ uint32_t chain_sparse_generic(const DevModel &m, int ktc
   return acc;
 }
 
-// Early-c merge of one output: S = S_p + aligned c, rounded in hardware.  A zero sum
-// is +0 when some product or c is nonzero; false for a zero sum of zero terms (its
-// sign needs the inputs) or a subnormal result.
-__device__ __forceinline__ bool merge_early(const DevModel &m, int32_t Sp, int32_t emax, uint32_t cb, bool have_p,
-                                            uint32_t &r) {
-  uint32_t cS, cneg;
-  int32_t cE;
-  decode_c(m, cb, cS, cE, cneg);
-  int32_t S = Sp;
-  if (cS) S += align_term<uint32_t, int32_t>(cS << m.P0c, cneg, emax + m.R0c - cE, 0);
+// Early-c merge of one output: S (products and c, aligned and truncated) rounded in
+// hardware.  A zero sum is +0 when some term is nonzero; false for a zero sum of zero
+// terms (its sign needs the inputs) or a subnormal result.
+__device__ __forceinline__ bool merge_early(const DevModel &m, int32_t S, int32_t emax, bool have_nz, uint32_t &r) {
   if (S == 0) {
     r = 0u;
-    return have_p || cS != 0u;
+    return have_nz;
   }
   return hw_round32(S, emax - m.F, m.rne, r);
 }
@@ -282,17 +276,20 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
 #pragma unroll
           for (int b = 0; b < kFT; b++) {
             int32_t em = emax[a][b];
+            Sp[a][b] = 0;
             if constexpr (ARCH == MCEMU_ARCH_GA_EARLY) {
-              const uint32_t cb = acc[a][b];
-              const uint32_t ef = (cb >> 23) & 0xFFu, mf = cb & 0x7FFFFFu;
-              const bool cz = (ef == 0u) && ((mf & m.c_sub_keep) == 0u);
-              const int32_t ec = cz ? m.c_zero_exp : (int32_t)max(ef, 1u) - 127;
+              // c joins e_max and is aligned here, so the sum starts with its term
+              uint32_t cS, cneg;
+              int32_t cE;
+              decode_c(m, acc[a][b], cS, cE, cneg);
+              const int32_t ec = cS ? cE : m.c_zero_exp;
               em = max(max(em, ec), m.emin_lim);
-              if (emax[a][b] > -1024) hpm |= 1u << (a * kFT + b);   // some product is nonzero
+              if (emax[a][b] > -1024 || cS) hpm |= 1u << (a * kFT + b);   // a nonzero term
               emax[a][b] = em;
+              if (cS)                                     // truncation (the kernel takes no RD model)
+                Sp[a][b] = (int32_t)shr32(cS * m.p0cmul, em + m.R0c - cE) * (1 - 2 * (int32_t)cneg);
             }
             base[a][b] = em + m.R0;
-            Sp[a][b] = 0;
           }
         // ---- pass 2: aligned, truncated products
         for (int q = b0; q < b0 + nt; q++) {
@@ -325,7 +322,7 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
                         (m.prod_ovf && emax[a][b] >= 126));
             if (ok) {
               if constexpr (ARCH == MCEMU_ARCH_GA_EARLY)
-                ok = merge_early(m, Sp[a][b], emax[a][b], cb, (hpm >> (a * kFT + b)) & 1u, r);
+                ok = merge_early(m, Sp[a][b], emax[a][b], (hpm >> (a * kFT + b)) & 1u, r);
               else ok = merge_late(m, Sp[a][b], emax[a][b], cb, r);
             }
             if (!ok) redo |= 1u << (a * kFT + b);
