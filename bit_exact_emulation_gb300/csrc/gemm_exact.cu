@@ -142,10 +142,10 @@ __global__ void __launch_bounds__(kFThreads, 1) gemm_exact_kernel(const __grid_c
             if (st[a][b] == 0u && w == 0)                    // exact zero: +0 unless every term is zero
               ok = ok && ((nzm >> (a * kFT + b)) & 1u);
             else if (st[a][b] == 0u)                         // the window holds the exact sum
-              ok = ok && hw_round64(w, L, m.rne, lo);
+              ok = ok && hw_round64_1(w, L, m.rne, lo);
             else
-              ok = ok && (w >= (1ll << 26) || w <= -(1ll << 26)) && hw_round64(4 * w, L - 2, m.rne, lo) &&
-                   hw_round64(4 * (w + nt + 1) - 1, L - 2, m.rne, hi) && lo == hi;
+              ok = ok && (w >= (1ll << 26) || w <= -(1ll << 26)) && hw_round64_1(4 * w, L - 2, m.rne, lo) &&
+                   hw_round64_1(4 * (w + nt + 1) - 1, L - 2, m.rne, hi) && lo == hi;
             if (!ok) redo |= 1u << (a * kFT + b);
             acc[a][b] = lo;
           }

@@ -140,7 +140,7 @@ __device__ __forceinline__ bool merge_early(const DevModel &m, int32_t S, int32_
     r = 0u;
     return have_nz;
   }
-  return hw_round32(S, emax - m.F, m.rne, r);
+  return hw_round32_1(S, emax - m.F, m.rne, r);
 }
 
 // Algorithm 1, lines 5-15, for one output with hardware rounding.  A zero sum is +0
@@ -166,7 +166,7 @@ __device__ __forceinline__ bool merge_late(const DevModel &m, int32_t Sp, int32_
       r = 0u;
       return true;
     }
-    return hw_round32(Sacc, emax - m.F, m.rne, r);      // line 15
+    return hw_round32_1(Sacc, emax - m.F, m.rne, r);      // line 15
   }
   // line 10: S_p on c's grid with RD (floor) at psum_frac fraction bits; in this branch
   // e_max < e_c, so the shift is at least 1 - (psum_frac - F_p) >= -8 and the product
@@ -188,7 +188,7 @@ __device__ __forceinline__ bool merge_late(const DevModel &m, int32_t Sp, int32_
     Sacc >>= min(rsh, 63);                               // floor = RD for either sign
     lsb += rsh;
   }
-  return hw_round64(Sacc, lsb, m.rne, r);                // line 15
+  return hw_round64_1(Sacc, lsb, m.rne, r);                // line 15
 }
 
 // A NaN pattern no model returns (their NaN results are always nan_bits): it marks
