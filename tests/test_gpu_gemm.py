@@ -283,6 +283,22 @@ def test_multiword_gemm_word_counts(L, n_words):
         assert np.array_equal(D.view(np.uint64), want.view(np.uint64))
 
 
+def test_multiword_fp64_4096_sampled(L):
+    """The multi-word workload at full size (4096^3, 3 words, 9 and 6 products, CDNA3 BF16
+    word model): sampled entries against the oracle."""
+    M = N = K = 4096
+    A, Bt = W.gen_multiword_fp64(M, N, K, seed=5)
+    m = L.Model(PRESETS["cdna3_bf16"])
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(Bt).cuda()
+    rng = np.random.default_rng(13)
+    ii = rng.integers(0, M, 24).astype(np.int32)
+    jj = rng.integers(0, N, 24).astype(np.int32)
+    for truncated in (False, True):
+        D = L.multiword_gemm(m, L.tile(0, 32, 32, 8, 4), 3, truncated, dA, dB).cpu().numpy()
+        want = oracle.multiword_entries(PRESETS["cdna3_bf16"], 8, 3, truncated, A, Bt, ii, jj)
+        assert np.array_equal(D[ii, jj].view(np.uint64), want.view(np.uint64))
+
+
 def test_multiword_error_report(L):
     M, N, K = 64, 48, 256
     A, Bt = W.gen_multiword_fp64(M, N, K, seed=7)

@@ -123,6 +123,20 @@ def test_full_size_sampled(L, fmt, k, enc):
         assert np.array_equal(got, want), f"{fmt} {name}\n" + mismatches(got, want)
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("enc", ["ocp", "fnuz"])
+@pytest.mark.parametrize("k", [8, 16, 32])
+def test_fp8_table_kernel_encodings_and_block_sizes(L, fmt, enc, k):
+    """The FP8 product-table kernel for both encodings and the block sizes it serves,
+    global alignment (truncate, RNE) and exact-then-round, specials included."""
+    a, b, c = W.gen_block_fma_set(fmt, 30000, k, seed=50 + k, enc=enc, special_rate=0.01)
+    for name, spec in block_models(fmt, k).items():
+        spec = dict(spec, fp8_enc=enc)
+        got = gpu_block(L, spec, a, b, c)
+        want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+        assert np.array_equal(got, want), f"{fmt} {enc} k={k} {name}\n" + mismatches(got, want)
+
+
 # exponent-mantissa sampling (Algorithm 3, seed 0) at the exponent limits of Sec. 5.1
 CDNA3_SAMPLING = [
     ("cdna3_fp16", "fp16", (-14, 15), (-126, 127)), ("cdna3_fp16", "fp16", (-24, -14), (-149, -126)),
