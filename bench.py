@@ -21,6 +21,7 @@ import subprocess
 import sys
 import threading
 import time
+from fractions import Fraction
 
 import numpy as np
 
@@ -261,13 +262,34 @@ def gemm_multiword(L, torch, timed, steps):
     ws = torch.empty(L.multiword_workspace(3, M, N, K), dtype=torch.uint8, device="cuda")
     D = torch.empty((M, N), dtype=torch.float64, device="cuda")
     R = dA @ dB.T
+    # exact values of 256 sampled entries: every binary64 product is an integer times a
+    # power of two, so the dot product is summed exactly in Python integers
+    rng = np.random.default_rng(21)
+    si, sj = rng.integers(0, M, 256), rng.integers(0, N, 256)
+    exact = [exact_dot(A[i], Bt[j]) for i, j in zip(si, sj)]
     mw = {}
     for label, trunc, npairs in (("9_products", False, 9), ("6_products", True, 6)):
         sec = timed(lambda: L.multiword_gemm(m, t, 3, trunc, dA, dB, D, ws), max(1, steps // 2))
         e2, r2 = L.fro_error(D, R).cpu().numpy()
+        Dh = D.cpu().numpy()
+        rel = [abs(Fraction(float(Dh[i, j])) - x) / abs(x) for (i, j), x in zip(zip(si, sj), exact) if x != 0]
         mw[label] = {"ms": sec * 1e3, "gflops_emulated": npairs * 2.0 * M * N * K / sec / 1e9,
-                     "rel_fro_error": float(np.sqrt(e2 / r2))}
+                     "rel_fro_error": float(np.sqrt(e2 / r2)),
+                     "rel_err_exact_sampled": {"max": float(max(rel)), "median": float(np.median([float(r) for r in rel])),
+                                               "entries": len(rel)}}
     return mw
+
+
+def exact_dot(x, y):
+    """Exact sum of x[k] * y[k] for binary64 vectors, as a Fraction."""
+    terms = []
+    for u, v in zip(x.tolist(), y.tolist()):
+        pu, qu = u.as_integer_ratio()
+        pv, qv = v.as_integer_ratio()
+        terms.append((pu * pv, qu * qv))
+    den = max(q for _, q in terms)                  # denominators are powers of two
+    num = sum(p * (den // q) for p, q in terms)
+    return Fraction(num, den)
 
 
 def main():
