@@ -38,6 +38,14 @@ VEC_BYTES = {f: k * (1 if f in ("e4m3", "e5m2", "int8") else (2 if f in ("fp16",
              for f, k in FORMATS}
 
 
+def workload_config(n_vec):
+    """The workload both arms report (the reference arm times a bounded sample of it)."""
+    return {"workload": f"randomized block-FMA vector sets: {n_vec:.0e} each of FP16 K=4, BF16 K=4, XF32 K=2, "
+                        "E4M3 K=8, E5M2 K=8 (OCP) x {truncate, RNE, exact} + INT8 K=16",
+            "vector_sets_per_step_per_gpu": n_vec * 16, "launches_per_step": 16,
+            "l2": "inputs larger than L2 (200-400 MB read per launch)"}
+
+
 def rank_seed(k, rank):
     """Seed of one rank's vector sets: every rank streams its own sets (weak scaling)."""
     return 2 + k + 1000 * rank
@@ -156,7 +164,7 @@ def run_reference(args, rank):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "block-FMA/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int (exact big-integer)",
-            "data": "synthetic", "config": {"workload": "randomized block-FMA vector sets (bounded sample)"},
+            "data": "synthetic", "config": workload_config(N_VEC),
             "cpu_baseline": {"value": value, "unit": "block-FMA/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "block-FMA/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -447,11 +455,7 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": "block-FMA/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int32/int64 integer significand arithmetic", "data": "synthetic",
-            "config": {"workload": f"randomized block-FMA vector sets: {n_vec:.0e} each of FP16 K=4, BF16 K=4, XF32 K=2, "
-                                   "E4M3 K=8, E5M2 K=8 (OCP) x {truncate, RNE, exact} + INT8 K=16",
-                       "vector_sets_per_step_per_gpu": fmas_per_step, "launches_per_step": len(launches),
-                       "l2": "inputs larger than L2 (200-400 MB read per launch)",
-                       "parity_sample_mismatches": mism, "parity_sample": n_cpu},
+            "config": dict(workload_config(n_vec), parity_sample_mismatches=mism, parity_sample=n_cpu),
             "gpu_launches": len(launches) * args.steps, "clocks": clk, "roofline": roofline,
             "cpu_baseline": cpu, "e2e": e2e, "gemm": gemm}
     print(json.dumps(line), flush=True)
