@@ -136,14 +136,28 @@ __global__ void __launch_bounds__(kStreamThreads) fast_kernel(const __grid_const
   size_t *q = queue[warp];
   int qn = 0;                                          // warp-uniform queue length
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t base = (size_t)blockIdx.x * blockDim.x + (size_t)warp * 32; base < n; base += stride) {
+  // software pipeline: the next vector set's words are loaded while this one is evaluated
+  uint32_t na[NW], nb[NW], nc = 0;
+  size_t base = (size_t)blockIdx.x * blockDim.x + (size_t)warp * 32;
+  if (base + lane < n) {
+    load_words<NB>(a + (base + lane) * NB, na);
+    load_words<NB>(b + (base + lane) * NB, nb);
+    nc = __ldcs(c + base + lane);
+  }
+  for (; base < n; base += stride) {
     const size_t v = base + lane;
+    uint32_t wa[NW], wb[NW];
+#pragma unroll
+    for (int i = 0; i < NW; i++) { wa[i] = na[i]; wb[i] = nb[i]; }
+    const uint32_t cb = nc;
+    const size_t vn = v + stride;
+    if (vn < n) {
+      load_words<NB>(a + vn * NB, na);
+      load_words<NB>(b + vn * NB, nb);
+      nc = __ldcs(c + vn);
+    }
     bool special = false;
     if (v < n) {
-      uint32_t wa[NW], wb[NW];
-      load_words<NB>(a + v * NB, wa);
-      load_words<NB>(b + v * NB, wb);
-      const uint32_t cb = __ldcs(c + v);
       uint32_t sw = (cb & 0x7F800000u) == 0x7F800000u;
 #pragma unroll
       for (int i = 0; i < NW; i++) sw |= fspecial_word<ID>(wa[i]) | fspecial_word<ID>(wb[i]);
