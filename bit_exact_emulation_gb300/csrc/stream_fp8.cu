@@ -262,16 +262,26 @@ __global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant
   const uint16_t *tab = reinterpret_cast<const uint16_t *>(f8_smem);
   constexpr int NW = K / 4;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
-    uint32_t wa[NW], wb[NW];
+  // software pipeline: the next vector set's words are loaded while this one is evaluated
+  uint32_t na[NW], nb[NW], nc = 0;
+  auto load = [&](size_t u) {
 #pragma unroll
     for (int w = 0; w < NW; w += 2) {
-      const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(a + v * K) + w / 2);
-      const uint2 y = __ldcs(reinterpret_cast<const uint2 *>(b + v * K) + w / 2);
-      wa[w] = x.x; wa[w + 1] = x.y;
-      wb[w] = y.x; wb[w + 1] = y.y;
+      const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(a + u * K) + w / 2);
+      const uint2 y = __ldcs(reinterpret_cast<const uint2 *>(b + u * K) + w / 2);
+      na[w] = x.x; na[w + 1] = x.y;
+      nb[w] = y.x; nb[w + 1] = y.y;
     }
-    const uint32_t cb = __ldcs(c + v);
+    nc = __ldcs(c + u);
+  };
+  size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (v < n) load(v);
+  for (; v < n; v += stride) {
+    uint32_t wa[NW], wb[NW];
+#pragma unroll
+    for (int w = 0; w < NW; w++) { wa[w] = na[w]; wb[w] = nb[w]; }
+    const uint32_t cb = nc;
+    if (v + stride < n) load(v + stride);
     uint32_t e[K], sg[K];
     f8_lookup<K>(tab, wa, wb, e, sg);
     uint32_t mx = 0, orv = 0;
