@@ -57,10 +57,24 @@ __global__ void __launch_bounds__(256) block_int_kernel(const __grid_constant__ 
                                                         uint32_t *__restrict__ d) {
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   const bool ss = m.fa.is_signed && m.fb.is_signed, uu = !m.fa.is_signed && !m.fb.is_signed;
-  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
+  // software pipeline: the next vector set is loaded while this one is reduced
+  uint32_t na[KM / 4], nb[KM / 4], nc = 0;
+  size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (v < n) {
+    load_words<KM>(a + v * KM, na);
+    load_words<KM>(b + v * KM, nb);
+    nc = __ldcs(c + v);
+  }
+  for (; v < n; v += stride) {
     uint32_t wa[KM / 4], wb[KM / 4];
-    load_words<KM>(a + v * KM, wa);
-    load_words<KM>(b + v * KM, wb);
+#pragma unroll
+    for (int i = 0; i < KM / 4; i++) { wa[i] = na[i]; wb[i] = nb[i]; }
+    const uint32_t cb = nc;
+    if (v + stride < n) {
+      load_words<KM>(a + (v + stride) * KM, na);
+      load_words<KM>(b + (v + stride) * KM, nb);
+      nc = __ldcs(c + v + stride);
+    }
     int32_t s = 0;       // exact: |sum| <= 32 * 255 * 255
     if (ss) {
 #pragma unroll
@@ -74,7 +88,6 @@ __global__ void __launch_bounds__(256) block_int_kernel(const __grid_constant__ 
       split_elems<1, KM>(wb, eb, KM);
       s = (int32_t)block_int<KM>(m, ea, eb, KM, 0u);
     }
-    uint32_t cb = __ldcs(c + v);
     uint32_t r;
     if (m.int_sat) {
       int64_t t = (int64_t)s + (int64_t)(int32_t)cb;
