@@ -17,7 +17,7 @@
 namespace mcemu {
 
 template <int ESZ, int SPARSE>
-__global__ void __launch_bounds__(kFThreads, 1) gemm_exact_kernel(const __grid_constant__ DevModel m, int kt,
+__global__ void __launch_bounds__(kFThreads, 2) gemm_exact_kernel(const __grid_constant__ DevModel m, int kt,
                                                                 int kblk, int logk, int M, int N, int K,
                                                                 const uint8_t *__restrict__ A, int64_t lda,
                                                                 const uint8_t *__restrict__ meta, int64_t ldm,
