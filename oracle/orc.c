@@ -527,7 +527,10 @@ static uint32_t block_eval(const orc_model *md, int n, const uint32_t *a, const 
     p[l] = make_product(md, decode_in(md, md->fmt_a, a[l]), decode_in(md, md->fmt_b, b[l]));
   cc = make_c(md, c);
   uint32_t d;
-  if (special_result(md, p, n, &cc, &d)) return d;
+  /* The pair-wise model is a sequence of fp32 operations (Sec. 4.2): an fl() that
+   * overflows creates an infinity that then meets the inputs' infinities under
+   * the IEEE rules, so its special values are resolved inside arch_pairwise. */
+  if (md->arch != ORC_PAIRWISE && special_result(md, p, n, &cc, &d)) return d;
   switch (md->arch) {
     case ORC_EXACT: return arch_exact(md, p, n, &cc);
     case ORC_GA_EARLY: return arch_ga_early(md, p, n, &cc);

@@ -1,0 +1,109 @@
+"""Seeded fuzzing of the model space: random valid model descriptors (every
+architecture, format pairing, rounding, flush and exponent-limit option the
+descriptor allows), each run through the block-FMA stream and the tile GEMM on the
+GPU and compared bit for bit with the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from bit_exact_emulation_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+BY_SIZE = {1: ["e4m3", "e5m2"], 2: ["fp16", "bf16"], 4: ["xf32", "fp32"]}
+
+
+def random_spec(rng):
+    size = int(rng.choice([1, 2, 4]))
+    fa = str(rng.choice(BY_SIZE[size]))
+    fb = fa if rng.random() < 0.7 else str(rng.choice(BY_SIZE[size]))
+    arch = str(rng.choice(["exact", "ga_early", "ga_late", "odd_even", "pairwise"]))
+    k = int(rng.choice([1, 2, 3, 4, 5, 8, 12, 16, 24, 32]))
+    flush = bool(rng.random() < 0.3)
+    spec = dict(fmt_a=fa, fmt_b=fb, arch=arch, n_fma=k, fp8_enc=str(rng.choice(["ocp", "fnuz"])),
+                xf32_round=str(rng.choice(["trunc", "rne"])), out_round=str(rng.choice(["rne", "rtz"])),
+                align_round=str(rng.choice(["rz", "rd"])), sub_in_flush=flush,
+                sub_out_flush=bool(rng.random() < 0.3), c_zero_exp=[None, -126][int(rng.integers(0, 2))],
+                prod_overflow=bool(rng.random() < 0.5), nan_bits=int(rng.choice([0x7FC00000, 0xFFC00000])),
+                pair_group=k)
+    if arch == "ga_early":
+        spec["align_frac"] = int(rng.integers(8, 53))
+        spec["emin_lim"] = [None, int(rng.integers(-140, -118))][int(rng.integers(0, 2))]
+    if arch in ("ga_late", "odd_even"):
+        F = int(rng.integers(14, 31))
+        spec.update(align_frac=F, c_frac=F, psum_frac=int(rng.integers(max(23, F), F + 9)),
+                    post_norm_frac=int(rng.integers(23, 41)))
+    if arch == "pairwise":
+        spec.update(sub_out_flush=flush, out_round="rne")
+    return spec
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_exact_emulation_gb300 import build
+    build.build()
+    from bit_exact_emulation_gb300 import binding
+    return binding
+
+
+def dev(x):
+    x = np.ascontiguousarray(x)
+    return torch.from_numpy(x.view({np.uint16: np.int16, np.uint32: np.int32}.get(x.dtype.type, x.dtype))).cuda()
+
+
+def operands(rng, spec, shape_a, shape_b, shape_c, rate):
+    enc = spec["fp8_enc"]
+    a = W.independent_bits(rng, spec["fmt_a"], shape_a, enc, rate)
+    b = W.independent_bits(rng, spec["fmt_b"], shape_b, enc, rate)
+    c = W.independent_bits(rng, "fp32", shape_c, "ocp", rate)
+    return a, b, c
+
+
+def model_or_skip(L, spec):
+    try:
+        return L.Model(spec)
+    except L.McemuError:
+        return None
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fuzz_block_fma(L, seed):
+    rng = np.random.default_rng(1000 + seed)
+    ran = 0
+    for _ in range(8):
+        spec = random_spec(rng)
+        m = model_or_skip(L, spec)
+        if m is None:
+            continue
+        k = spec["n_fma"]
+        a, b, c = operands(rng, spec, (3000, k), (3000, k), (3000,), float(rng.choice([0.0, 0.01, 0.05])))
+        got = L.block_fma(m, dev(a), dev(b), dev(c)).cpu().numpy().view(np.uint32)
+        want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+        bad = np.nonzero(got != want)[0]
+        assert len(bad) == 0, f"{spec}: {len(bad)} differ, first {bad[0]}: gpu {got[bad[0]]:#010x} oracle {want[bad[0]]:#010x}"
+        ran += 1
+    assert ran > 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fuzz_tile_gemm(L, seed):
+    rng = np.random.default_rng(2000 + seed)
+    ran = 0
+    for _ in range(4):
+        spec = random_spec(rng)
+        m = model_or_skip(L, spec)
+        if m is None:
+            continue
+        kt = int(rng.choice([spec["n_fma"], 2 * spec["n_fma"], 8, 16, 32]))
+        M, N, K = int(rng.integers(1, 70)), int(rng.integers(1, 70)), int(rng.integers(1, 90))
+        A, Bt, C = operands(rng, spec, (M, K), (N, K), (M, N), float(rng.choice([0.0, 0.005])))
+        D = L.tile_gemm(m, L.tile(0, 16, 16, kt, 4), dev(A), dev(Bt), dev(C)).cpu().numpy().view(np.uint32)
+        ii, jj = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+        want = oracle.gemm_entries(spec, K, kt, A, Bt, C, ii.ravel().astype(np.int32),
+                                   jj.ravel().astype(np.int32)).reshape(M, N)
+        assert np.array_equal(D, want), f"{spec} kt={kt} M={M} N={N} K={K}: {int((D != want).sum())} differ"
+        ran += 1
+    assert ran > 0

@@ -268,6 +268,24 @@ def test_power_of_two_scaling(preset):
     assert np.array_equal(d2[nz], d[nz] + np.uint32(s << 23))
 
 
+def test_pairwise_k1_is_ieee_fp32():
+    """The pair-wise model with one product and no flushing is fl(c + fl(a * b)) in IEEE
+    fp32 (Sec. 4.2): numpy's float32 arithmetic gives the same bits, including products
+    that overflow to an infinity and then meet an infinite c."""
+    rng = np.random.default_rng(8)
+    n = 20000
+    a = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+    b = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+    c = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+    c[::7] = np.where(rng.random(len(c[::7])) < 0.5, 0x7F800000, 0xFF800000)
+    spec = dict(fmt_a="fp32", fmt_b="fp32", arch="pairwise", n_fma=1, pair_group=1, nan_bits=0x7FC00000)
+    got = oracle.block_fma(spec, a.reshape(n, 1), b.reshape(n, 1), c)
+    with np.errstate(all="ignore"):
+        ref = (c.view(np.float32) + a.view(np.float32) * b.view(np.float32)).astype(np.float32)
+    want = np.where(np.isnan(ref), np.uint32(0x7FC00000), ref.view(np.uint32))
+    assert np.array_equal(got, want)
+
+
 def test_int8_is_integer_dot_product():
     rng = np.random.default_rng(2)
     for fa, fb in (("int8", "int8"), ("uint8", "uint8")):
