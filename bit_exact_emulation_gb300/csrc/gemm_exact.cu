@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_exact_kernel(const __grid_c
         int32_t C1[kFT][kFT];
         uint32_t st[kFT][kFT];                               // nonzero once a term lost bits
         uint32_t nzm = 0;                                    // outputs with a nonzero product or c
+        uint32_t ovm = 0;                                    // outputs whose products may reach 2^128
 #pragma unroll
         for (int a = 0; a < kFT; a++)
 #pragma unroll
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_exact_kernel(const __grid_c
             int32_t cE;
             decode_c(m, acc[a][b], cS, cE, cneg);
             if (T[a][b] > -1024 || cS) nzm |= 1u << (a * kFT + b);
+            if (m.prod_ovf && T[a][b] >= 126) ovm |= 1u << (a * kFT + b);   // CDNA 3 product overflow
             int32_t top = T[a][b] + 2;                       // products: |p| < 2^(E_a + E_b + 2)
             if (cS) top = max(top, cE + 1);
             const int32_t L = top - 61 + logk;
@@ -137,7 +139,8 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_exact_kernel(const __grid_c
             const int64_t w = W[a][b];
             const int32_t L = T[a][b];
             uint32_t lo = 0, hi = 1;
-            bool ok = !((((rowsp >> a) | (colsp >> b)) & 1u) || (acc[a][b] & 0x7F800000u) == 0x7F800000u) &&
+            bool ok = !((((rowsp >> a) | (colsp >> b)) & 1u) || (acc[a][b] & 0x7F800000u) == 0x7F800000u ||
+                        ((ovm >> (a * kFT + b)) & 1u)) &&
                       L > kNegE / 2;
             if (st[a][b] == 0u && w == 0)                    // exact zero: +0 unless every term is zero
               ok = ok && ((nzm >> (a * kFT + b)) & 1u);

@@ -31,7 +31,7 @@ def random_spec(rng):
         spec["align_frac"] = int(rng.integers(8, 53))
         spec["emin_lim"] = [None, int(rng.integers(-140, -118))][int(rng.integers(0, 2))]
     if arch in ("ga_late", "odd_even"):
-        F = int(rng.integers(14, 31))
+        F = int(rng.integers(15, 31))              # psum_frac in [max(23, F), F + 8] must exist
         spec.update(align_frac=F, c_frac=F, psum_frac=int(rng.integers(max(23, F), F + 9)),
                     post_norm_frac=int(rng.integers(23, 41)))
     if arch == "pairwise":
