@@ -281,28 +281,34 @@ __device__ __forceinline__ AT align_term(UT Ushift, uint32_t neg, int32_t sh, in
   }
 }
 
-template <class AT>
+// RM: the output rounding fixed at compile time (1 = RNE, 0 = toward zero), or -1 to
+// read it from the model
+template <int RM>
+__device__ __forceinline__ int out_rne(const DevModel &m) { return RM >= 0 ? RM : m.rne; }
+
+template <class AT, int RM = -1>
 __device__ __forceinline__ uint32_t pack_sum(AT S, int32_t lsb, const DevModel &m) {
+  const int rne = out_rne<RM>(m);
   if (!m.sub_out_flush) {
     uint32_t bits;
-    const bool ok = (sizeof(AT) == 4) ? hw_round32((int32_t)S, lsb, m.rne, bits)
-                                      : hw_round64((int64_t)S, lsb, m.rne, bits);
+    const bool ok = (sizeof(AT) == 4) ? hw_round32((int32_t)S, lsb, rne, bits)
+                                      : hw_round64((int64_t)S, lsb, rne, bits);
     if (ok) return bits;
   }
   uint32_t neg = S < 0 ? 1u : 0u;
   if (sizeof(AT) == 4) {
     uint32_t M = neg ? (uint32_t)(-(int32_t)S) : (uint32_t)S;
-    return round_pack32(M, lsb, neg, m.rne, m.sub_out_flush);
+    return round_pack32(M, lsb, neg, rne, m.sub_out_flush);
   }
   uint64_t M = neg ? (uint64_t)(-(int64_t)S) : (uint64_t)S;
-  return round_pack(M, lsb, neg, false, m.rne, m.sub_out_flush);
+  return round_pack(M, lsb, neg, false, rne, m.sub_out_flush);
 }
 
 // ---------------------------------------------------------------------------
 // GA_EARLY: global alignment with c aligned together with the products
 // (Table 3, early c; e_{c=0} and e_min^lim as configured).
 // ---------------------------------------------------------------------------
-template <int K, class UT, class AT>
+template <int K, class UT, class AT, int RM = -1>
 __device__ __forceinline__ uint32_t arch_ga_early(const DevModel &m, const Term<UT> (&p)[K], int nt,
                                                   uint32_t cS, int32_t cE, uint32_t cneg) {
   int32_t emax = m.emin_lim;
@@ -330,7 +336,7 @@ __device__ __forceinline__ uint32_t arch_ga_early(const DevModel &m, const Term<
     if (cS) S += align_term<UT, AT>((UT)cS << m.P0c, cneg, emax + m.R0c - cE, m.align_rd);
   }
   if (S == 0) return zero_result<K, UT>(p, nt, cS, cneg);
-  return pack_sum<AT>(S, emax - m.F, m);
+  return pack_sum<AT, RM>(S, emax - m.F, m);
 }
 
 // ---------------------------------------------------------------------------
@@ -636,14 +642,15 @@ __device__ __forceinline__ bool merge_c64(const DevModel &m, int64_t Wt, int32_t
          hw_round64(4 * (S + nb) - 1, L - 2, m.rne, hi) && out == hi;
 }
 
-template <int K, class UT>
-__device__ __forceinline__ uint32_t arch_exact64(const DevModel &m, const Term<UT> (&p)[K], uint32_t cS,
-                                                 int32_t cE, uint32_t cneg) {
+// False when the window does not decide the rounding (out is then unset).
+template <int K, class UT, int RM = -1>
+__device__ __forceinline__ bool arch_exact64_try(const DevModel &m, const Term<UT> (&p)[K], uint32_t cS,
+                                                 int32_t cE, uint32_t cneg, uint32_t &out) {
   int32_t T = kNegE;
 #pragma unroll
   for (int l = 0; l < K; l++) T = max(T, p[l].e + 2);
   if (cS) T = max(T, cE + 1);
-  if (T <= kNegE / 2) return zero_result<K, UT>(p, K, cS, cneg);
+  if (T <= kNegE / 2) { out = zero_result<K, UT>(p, K, cS, cneg); return true; }
   const int32_t L = T - 61 + ExactLog<K>::v;
   const int32_t QP = 60 - m.mab;                     // products: |U| < 2^(mab + 2)
   int64_t W = 0;
@@ -654,23 +661,42 @@ __device__ __forceinline__ uint32_t arch_exact64(const DevModel &m, const Term<U
     exact64_add<K>(W, nb, sv, QP, QP - (p[l].e - m.mab) + L);
   }
   if (cS) exact64_add<K>(W, nb, cneg ? -(int32_t)cS : (int32_t)cS, 38, 38 - (cE - 23) + L);
+  // The sum is W units when nb == 0, else it lies in (W, W + nb).  With |W| >= 2^26,
+  // W + 1/2 and W + nb - 1/2 (2W + 1 and 2(W + nb) - 1 in units of 2^(L-1)) round like
+  // every value next to them; for nb == 0 both ends are 2W.  So one branch-free
+  // bracket serves both cases; the rest (zero, subnormal or flushed results, dropped
+  // bits under heavy cancellation) is rare.
+  const int rne = out_rne<RM>(m);
+  const int64_t z = nb ? 1 : 0;
+  const int64_t X = 2 * W + z, Y = 2 * (W + nb) - z;
+  const bool big = W >= (1ll << 26) || W <= -(1ll << 26);
   uint32_t lo, hi;
+  if ((big || (nb == 0 && W != 0)) && !m.sub_out_flush) {
+    const bool okx = hw_round64(X, L - 1, rne, lo), oky = hw_round64(Y, L - 1, rne, hi);
+    if (okx && oky) {
+      if (lo == hi) { out = lo; return true; }
+      return false;            // both ends correctly rounded and different: undecided
+    }
+  }
   if (nb == 0) {
-    if (W == 0) return zero_result<K, UT>(p, K, cS, cneg);
-    if (!m.sub_out_flush && hw_round64(W, L, m.rne, lo)) return lo;
+    if (W == 0) { out = zero_result<K, UT>(p, K, cS, cneg); return true; }
     // subnormal or flushed result of an exact window: integer rounding
-    return round_pack(W < 0 ? 0ull - (uint64_t)W : (uint64_t)W, L, W < 0 ? 1u : 0u, false, m.rne, m.sub_out_flush);
+    out = round_pack(W < 0 ? 0ull - (uint64_t)W : (uint64_t)W, L, W < 0 ? 1u : 0u, false, rne, m.sub_out_flush);
+    return true;
   }
-  if (W >= (1ll << 26) || W <= -(1ll << 26)) {
-    // the sum lies in (W, W + nb): W + 1/2 and W + nb - 1/2 (2W + 1 and 2(W + nb) - 1 in
-    // units of 2^(L-1)) round like every value next to them
-    const int64_t X = 2 * W + 1, Y = 2 * (W + nb) - 1;
-    if (!m.sub_out_flush && hw_round64(X, L - 1, m.rne, lo) && hw_round64(Y, L - 1, m.rne, hi) && lo == hi)
-      return lo;
-    lo = round_pack(X < 0 ? 0ull - (uint64_t)X : (uint64_t)X, L - 1, X < 0 ? 1u : 0u, false, m.rne, m.sub_out_flush);
-    hi = round_pack(Y < 0 ? 0ull - (uint64_t)Y : (uint64_t)Y, L - 1, Y < 0 ? 1u : 0u, false, m.rne, m.sub_out_flush);
-    if (lo == hi) return lo;
+  if (big) {
+    lo = round_pack(X < 0 ? 0ull - (uint64_t)X : (uint64_t)X, L - 1, X < 0 ? 1u : 0u, false, rne, m.sub_out_flush);
+    hi = round_pack(Y < 0 ? 0ull - (uint64_t)Y : (uint64_t)Y, L - 1, Y < 0 ? 1u : 0u, false, rne, m.sub_out_flush);
+    if (lo == hi) { out = lo; return true; }
   }
+  return false;
+}
+
+template <int K, class UT>
+__device__ __forceinline__ uint32_t arch_exact64(const DevModel &m, const Term<UT> (&p)[K], uint32_t cS,
+                                                 int32_t cE, uint32_t cneg) {
+  uint32_t r;
+  if (arch_exact64_try<K, UT>(m, p, cS, cE, cneg, r)) return r;
   int64_t V[K + 1];
   int32_t Ls[K + 1];
   int n = 0;
@@ -1043,9 +1069,12 @@ __device__ __forceinline__ uint32_t fspecial_bits(const DevModel &m, const uint3
 }
 
 // One block FMA of K products, architecture and format fixed at compile time.
-template <int ARCH, int ID, int K, class UT, class AT>
+// With `slow` given, a set whose exact sum needs the full-width evaluator is not
+// evaluated: *slow is set and the result is left to the caller.
+template <int ARCH, int ID, int K, class UT, class AT, int RM = -1>
 __device__ __forceinline__ uint32_t block_fma_fast(const DevModel &m, const uint32_t (&ea)[K],
-                                                   const uint32_t (&eb)[K], uint32_t cbits, bool any_special) {
+                                                   const uint32_t (&eb)[K], uint32_t cbits, bool any_special,
+                                                   bool *slow = nullptr) {
   const uint32_t sk = m.fa.sub_keep;
   Term<UT> p[K];
 #pragma unroll
@@ -1062,13 +1091,19 @@ __device__ __forceinline__ uint32_t block_fma_fast(const DevModel &m, const uint
   uint32_t cS, cneg;
   int32_t cE;
   decode_c(m, cbits, cS, cE, cneg);
-  if constexpr (ARCH == MCEMU_ARCH_GA_EARLY) return arch_ga_early<K, UT, AT>(m, p, K, cS, cE, cneg);
+  if constexpr (ARCH == MCEMU_ARCH_GA_EARLY) return arch_ga_early<K, UT, AT, RM>(m, p, K, cS, cE, cneg);
   else if constexpr (ARCH == MCEMU_ARCH_GA_LATE) return arch_ga_late<K, UT, AT>(m, p, K, cS, cE, cneg);
   else if constexpr (ARCH == MCEMU_ARCH_ODD_EVEN) return arch_odd_even<K, UT, AT>(m, p, K, cS, cE, cneg);
   else if constexpr (ID == F_E4M3 || ID == F_E4M3Z || ID == F_E5M2 || ID == F_E5M2Z)
     return arch_exact_fixed<ID, K>(m, p, cS, cE, cneg, cbits);
-  else if constexpr (ID == F_FP16 || ID == F_BF16 || ID == F_XF32T || ID == F_XF32R)
+  else if constexpr (ID == F_FP16 || ID == F_BF16 || ID == F_XF32T || ID == F_XF32R) {
+    if (slow) {
+      uint32_t r = 0u;
+      if (!arch_exact64_try<K, UT, RM>(m, p, cS, cE, cneg, r)) *slow = true;
+      return r;
+    }
     return arch_exact64<K, UT>(m, p, cS, cE, cneg);
+  }
   else return arch_exact<K, UT>(m, p, K, cS, cE, cneg);
 }
 

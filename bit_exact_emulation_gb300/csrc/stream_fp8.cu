@@ -198,17 +198,15 @@ __device__ __forceinline__ int64_t mad_wide(int32_t a, int32_t b, int64_t c) {
 template <int ID, int K>
 __device__ __forceinline__ uint32_t f8_exact(const DevModel &m, const uint32_t (&e)[K], const uint32_t (&sg)[K],
                                              uint32_t cb, uint32_t mx) {
-  i128 W;
+  // the exact sum W = lo + hi * 2^31 (hi = 0 for E4M3), |lo|, |hi| < 2^42
+  int64_t lo = 0, hi = 0;
   if constexpr (Fmt<ID>::EB == 4) {
-    int64_t w = 0;
 #pragma unroll
     for (int l = 0; l < K; l++) {
       const int32_t sP = (int32_t)(((e[l] & 0xFFu) ^ sg[l]) - sg[l]);
-      w = mad_wide(sP, (int32_t)shl_clamp(1u, e[l] >> 10), w);      // X <= 29
+      lo = mad_wide(sP, (int32_t)shl_clamp(1u, e[l] >> 10), lo);     // X <= 29
     }
-    W = (i128)w;
   } else {
-    int64_t lo = 0, hi = 0;
 #pragma unroll
     for (int l = 0; l < K; l++) {
       const uint32_t X = e[l] >> 10;
@@ -216,34 +214,33 @@ __device__ __forceinline__ uint32_t f8_exact(const DevModel &m, const uint32_t (
       lo = mad_wide(sP, (int32_t)(shl_clamp(2u, X) >> 1), lo);      // 2^X for X <= 30, else 0
       hi = mad_wide(sP, (int32_t)shl_clamp(1u, X - 31u), hi);       // 2^(X-31) for X >= 31, else 0
     }
-    W = (i128)lo + ((i128)hi << 31);
+  }
+  // W in a 64-bit window: Wt * 2^Gw plus an unknown amount below it when stW.  hi * 2^31
+  // has no bits below 2^31, so W >> sh (sh <= 31) is hi * 2^(31 - sh) + (lo >> sh) exactly
+  // and only lo's low sh bits drop out; sh keeps |Wt| < 2^61.
+  constexpr int32_t G = F8<ID>::XMIN - F8<ID>::MAB - 1;
+  int64_t Wt = lo;
+  int32_t Gw = G, stW = 0, sh = 0;
+  if constexpr (Fmt<ID>::EB != 4) {
+    const uint64_t ah = hi < 0 ? 0ull - (uint64_t)hi : (uint64_t)hi;
+    sh = max(0, 64 - __clzll((long long)ah) - 29);
+    Wt = (int64_t)((uint64_t)hi << (31 - sh)) + (lo >> sh);
+    stW = (sh > 0 && (lo & ((1ll << sh) - 1)) != 0) ? 1 : 0;
+    Gw = G + sh;
   }
   uint32_t cS, cneg;
   int32_t cE;
   decode_c(m, cb, cS, cE, cneg);
-  if (W == 0) {
+  if (Wt == 0 && sh == 0) {                              // the products cancel exactly
     if (cS) return cb;                                  // c alone: already an fp32 value
     uint32_t all = cneg && mx == 0u ? 0xFFFFFFFFu : 0u;
 #pragma unroll
     for (int l = 0; l < K; l++) all &= sg[l];
     return all ? 0x80000000u : 0u;
   }
-  // the exact sum's top 62 bits (all of it for E4M3) and the addend in a 64-bit window
-  constexpr int32_t G = F8<ID>::XMIN - F8<ID>::MAB - 1;
-  int64_t Wt;
-  int32_t Gw = G, stW = 0;
-  if constexpr (Fmt<ID>::EB == 4) {
-    Wt = (int64_t)W;
-  } else {
-    const i128 aW = W < 0 ? -W : W;
-    const uint64_t top = (uint64_t)(aW >> 61);
-    const int32_t sh = top ? 64 - __clzll((long long)top) : 0;   // bits to drop
-    Wt = (int64_t)(W >> sh);
-    stW = (sh > 0 && (W & (((i128)1 << sh) - 1)) != 0) ? 1 : 0;
-    Gw = G + sh;
-  }
   uint32_t r;
   if (merge_c64(m, Wt, Gw, stW, cS, cE, cneg, r)) return r;
+  const i128 W = (i128)lo + ((i128)hi << 31);
   return exact_fixed_merge<ID>(m, W << 39, cS, cE, cneg, cb);
 }
 
