@@ -1068,18 +1068,13 @@ __device__ __forceinline__ uint32_t fspecial_bits(const DevModel &m, const uint3
   return spec;
 }
 
-// One block FMA of K products, architecture and format fixed at compile time.
-// With `slow` given, a set whose exact sum needs the full-width evaluator is not
-// evaluated: *slow is set and the result is left to the caller.
+// One block FMA from its K product terms, architecture and format fixed at compile
+// time; spec holds the special-value bits found so far.  With `slow` given, a set
+// whose exact sum needs the full-width evaluator is not evaluated: *slow is set and
+// the result is left to the caller.
 template <int ARCH, int ID, int K, class UT, class AT, int RM = -1>
-__device__ __forceinline__ uint32_t block_fma_fast(const DevModel &m, const uint32_t (&ea)[K],
-                                                   const uint32_t (&eb)[K], uint32_t cbits, bool any_special,
-                                                   bool *slow = nullptr) {
-  const uint32_t sk = m.fa.sub_keep;
-  Term<UT> p[K];
-#pragma unroll
-  for (int l = 0; l < K; l++) p[l] = fterm<ID, UT>(ea[l], eb[l], sk);
-  uint32_t spec = any_special ? fspecial_bits<ID, K>(m, ea, eb, cbits) : 0u;
+__device__ __forceinline__ uint32_t block_fma_terms(const DevModel &m, const Term<UT> (&p)[K], uint32_t cbits,
+                                                    uint32_t spec, bool *slow = nullptr) {
   if constexpr (ID == F_BF16 || ID == F_XF32T || ID == F_XF32R || ID == F_FP32) {
     if (m.prod_ovf) {
 #pragma unroll
@@ -1105,6 +1100,69 @@ __device__ __forceinline__ uint32_t block_fma_fast(const DevModel &m, const uint
     return arch_exact64<K, UT>(m, p, cS, cE, cneg);
   }
   else return arch_exact<K, UT>(m, p, K, cS, cE, cneg);
+}
+
+// One block FMA of K products from the elements' bit patterns.
+template <int ARCH, int ID, int K, class UT, class AT, int RM = -1>
+__device__ __forceinline__ uint32_t block_fma_fast(const DevModel &m, const uint32_t (&ea)[K],
+                                                   const uint32_t (&eb)[K], uint32_t cbits, bool any_special,
+                                                   bool *slow = nullptr) {
+  const uint32_t sk = m.fa.sub_keep;
+  Term<UT> p[K];
+#pragma unroll
+  for (int l = 0; l < K; l++) p[l] = fterm<ID, UT>(ea[l], eb[l], sk);
+  const uint32_t spec = any_special ? fspecial_bits<ID, K>(m, ea, eb, cbits) : 0u;
+  return block_fma_terms<ARCH, ID, K, UT, AT, RM>(m, p, cbits, spec, slow);
+}
+
+// Powers of two (and 2^22 - 1) for fterms_w16, passed in at run time so that the
+// compiler keeps them as multiplies (FMA pipe) instead of shifts and masks (ALU).
+struct W16Consts {
+  uint32_t one, two, k16, kmb, nzadd, nzmul;   // 1, 2, 2^16, 2^(32 - MB), 2^22 - 1, 2^10
+};
+
+// Product terms of K 16-bit elements (FP16 or BF16 with subnormals kept, no Inf or
+// NaN), two elements per 32-bit word.  Both halves of a word are decoded at once:
+// the exponent fields (mask), the hidden bits (the field plus the field mask carries
+// into bit 15 / 31 exactly when it is nonzero), the significands with their hidden
+// bits, and max(field, 1) for the subnormal exponent e_min.  The two products' field
+// sums come from one add.  Splitting the halves, the shifts by MB and the
+// zero-product case (e = kNegE) are multiplies by the constants in kc.
+template <int ID, int K, class UT>
+__device__ __forceinline__ void fterms_w16(const uint32_t *wa, const uint32_t *wb, Term<UT> (&p)[K],
+                                           const W16Consts &kc) {
+  using F = Fmt<ID>;
+  static_assert(F::BYTES == 2 && F::XF == 0 && K % 2 == 0, "16-bit formats, an even block size");
+  constexpr uint32_t EM2 = (F::EMASK << F::MB) * 0x10001u, MM2 = F::MMASK * 0x10001u;
+  constexpr uint32_t LSB2 = (1u << F::MB) * 0x10001u;
+  constexpr int SH = 15 - F::MB;
+  constexpr uint32_t C0 = (uint32_t)(-2 * F::BIAS - kNegE);   // e - kNegE = field sum + C0
+#pragma unroll
+  for (int i = 0; i < K / 2; i++) {
+    uint32_t Sw[2], Ep[2];
+#pragma unroll
+    for (int o = 0; o < 2; o++) {
+      const uint32_t w = o ? wb[i] : wa[i];
+      const uint32_t ef = w & EM2;
+      const uint32_t hs = ((ef + EM2) & 0x80008000u) >> SH;    // hidden bits at MB and MB + 16
+      Sw[o] = (w & MM2) | hs;
+      Ep[o] = ef | (~hs & LSB2);                               // max(field, 1) << MB per half
+    }
+    const uint32_t Es = Ep[0] + Ep[1];                          // (Ea' + Eb') << MB per half
+    const uint32_t Eh = __umulhi(Es, kc.k16), El = Es - Eh * kc.k16;
+    const uint32_t Sah = __umulhi(Sw[0], kc.k16), Sal = Sw[0] - Sah * kc.k16;
+    const uint32_t Sbh = __umulhi(Sw[1], kc.k16), Sbl = Sw[1] - Sbh * kc.k16;
+    const uint32_t X = wa[i] ^ wb[i];                           // product signs at bits 15, 31
+    const uint32_t Ul = Sal * Sbl, Uh = Sah * Sbh;               // < 2^22
+    const uint32_t nzl = __umulhi(Ul * kc.one + kc.nzadd, kc.nzmul);   // U != 0
+    const uint32_t nzh = __umulhi(Uh * kc.one + kc.nzadd, kc.nzmul);
+    p[2 * i].U = (UT)Ul;
+    p[2 * i].e = (int32_t)(nzl * (__umulhi(El, kc.kmb) + C0)) + kNegE;
+    p[2 * i].neg = __umulhi(X * kc.k16, kc.two);
+    p[2 * i + 1].U = (UT)Uh;
+    p[2 * i + 1].e = (int32_t)(nzh * (__umulhi(Eh, kc.kmb) + C0)) + kNegE;
+    p[2 * i + 1].neg = __umulhi(X, kc.two);
+  }
 }
 
 }  // namespace mcemu

@@ -143,9 +143,10 @@ __global__ void __launch_bounds__(kStreamThreads) fast_kernel(const __grid_const
                                                               const uint8_t *__restrict__ a,
                                                               const uint8_t *__restrict__ b,
                                                               const uint32_t *__restrict__ c,
-                                                              uint32_t *__restrict__ d) {
+                                                              uint32_t *__restrict__ d, const W16Consts kc) {
   constexpr int NB = KM * Fmt<ID>::BYTES;
   constexpr int NW = (NB + 3) / 4;
+  constexpr bool kWords = Fmt<ID>::BYTES == 2 && Fmt<ID>::XF == 0;   // packed 16-bit decode
   constexpr bool kDefer = ARCH == MCEMU_ARCH_EXACT && (ID == F_FP16 || ID == F_BF16 || ID == F_XF32T ||
                                                        ID == F_XF32R);
   __shared__ size_t queue[kStreamThreads / 32][64];
@@ -182,15 +183,22 @@ __global__ void __launch_bounds__(kStreamThreads) fast_kernel(const __grid_const
       for (int i = 0; i < NW; i++) sw |= fspecial_word<ID>(wa[i]) | fspecial_word<ID>(wb[i]);
       special = sw != 0u;
       if (!special) {
-        uint32_t ea[KM], eb[KM];
-#pragma unroll
-        for (int l = 0; l < KM; l++) {
-          ea[l] = felem<ID>(wa, l);
-          eb[l] = felem<ID>(wb, l);
-        }
         using UT = typename std::conditional<(WIDE || ID == F_FP32), uint64_t, uint32_t>::type;
         using AT = typename std::conditional<(WIDE || ID == F_FP32), int64_t, int32_t>::type;
-        const uint32_t r = block_fma_fast<ARCH, ID, KM, UT, AT, RM>(m, ea, eb, cb, false, kDefer ? &slow : nullptr);
+        uint32_t r;
+        if constexpr (kWords) {
+          Term<UT> p[KM];
+          fterms_w16<ID, KM, UT>(wa, wb, p, kc);
+          r = block_fma_terms<ARCH, ID, KM, UT, AT, RM>(m, p, cb, 0u, kDefer ? &slow : nullptr);
+        } else {
+          uint32_t ea[KM], eb[KM];
+#pragma unroll
+          for (int l = 0; l < KM; l++) {
+            ea[l] = felem<ID>(wa, l);
+            eb[l] = felem<ID>(wb, l);
+          }
+          r = block_fma_fast<ARCH, ID, KM, UT, AT, RM>(m, ea, eb, cb, false, kDefer ? &slow : nullptr);
+        }
         if (!slow) __stcs(d + v, r);
       }
     }
@@ -269,7 +277,8 @@ static int grid_for(size_t n, const void *kernel) {
   return (int)(want < 1 ? 1 : want);
 }
 
-typedef void (*FpKernel)(const DevModel, size_t, const uint8_t *, const uint8_t *, const uint32_t *, uint32_t *);
+typedef void (*FpKernel)(const DevModel, size_t, const uint8_t *, const uint8_t *, const uint32_t *, uint32_t *,
+                         const W16Consts);
 
 struct Special {
   int arch, id, km, wide, rm;                          // rm: output rounding, -1 = any
@@ -338,7 +347,9 @@ int launch_block_fma(const DevModel &m, size_t n, const void *a, const void *b, 
       if (m.arch != MCEMU_ARCH_EXACT && sp.wide != (m.wide != 0)) continue;
       if (sp.rm >= 0 && sp.rm != (m.rne != 0 ? 1 : 0)) continue;
       int grid = grid_for(n, (const void *)sp.fn);
-      sp.fn<<<grid, 256, 0, s>>>(m, n, (const uint8_t *)a, (const uint8_t *)b, c, d);
+      const uint32_t mb = id == F_FP16 ? 10u : 7u;                  // fterms_w16 (FP16, BF16)
+      const W16Consts kc{1u, 2u, 1u << 16, 1u << (32 - mb), (1u << 22) - 1u, 1u << 10};
+      sp.fn<<<grid, 256, 0, s>>>(m, n, (const uint8_t *)a, (const uint8_t *)b, c, d, kc);
       return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
     }
   }
