@@ -9,11 +9,13 @@
 //    passes over the block's k: the first takes e_max = max(E_a + E_b) with the
 //    fused add-max instruction, the second aligns and accumulates the products
 //    (IADD3 shift amount, IMAD product, funnel shift, IMAD signed accumulate);
-//  - the per-output merge with c and the rounding use the integer helpers of
-//    core.cuh with the hardware int->fp32 rounding.
-// An output whose chain meets an Inf/NaN input, an Inf/NaN accumulator, a possible
-// product overflow, an exact zero sum or a subnormal result is flagged and its
-// whole chain is evaluated again at the end with the general evaluator (rare; the
+//  - between blocks the accumulator is an integer-valued float f and a scale g
+//    (value f * 2^g): c is aligned by one exact multiply and a float->int conversion,
+//    and the block's rounding is the int->fp32 conversion, so no fp32 encode or
+//    decode runs per block.
+// An output whose chain meets an Inf/NaN input or addend, a possible product overflow,
+// a zero sum of zero terms, or a result outside the normal fp32 range is flagged, and
+// its whole chain is evaluated again at the end with the general evaluator (rare; the
 // result is the same model).
 #pragma once
 #include <cuda_runtime.h>
@@ -132,72 +134,13 @@ __device__ __noinline__ uint32_t chain_sparse_generic(const DevModel &m, int ktc
   return acc;
 }
 
-// Early-c merge of one output: S (products and c, aligned and truncated) rounded in
-// hardware.  A zero sum is +0 when some term is nonzero; false for a zero sum of zero
-// terms (its sign needs the inputs) or a subnormal result.
-__device__ __forceinline__ bool merge_early(const DevModel &m, int32_t S, int32_t emax, bool have_nz, uint32_t &r) {
-  if (S == 0) {
-    r = 0u;
-    return have_nz;
-  }
-  return hw_round32_1(S, emax - m.F, m.rne, r);
-}
-
-// Algorithm 1, lines 5-15, for one output with hardware rounding.  A zero sum is +0
-// when some product or c is nonzero; false for a zero sum of zero terms or a
-// subnormal result (the general evaluator then decides).
-__device__ __forceinline__ bool merge_late(const DevModel &m, int32_t Sp, int32_t emax, uint32_t cb, uint32_t &r) {
-  uint32_t cS, cneg;
-  int32_t cE;
-  decode_c(m, cb, cS, cE, cneg);
-  const bool have_p = emax > -1024;                      // zero products sit below -1900
-  const int32_t ec = cS ? cE : m.c_zero_exp;
-  const bool have_c = ec > kNegE / 2;
-  if (!have_p && !have_c) return false;
-  if (have_p && (!have_c || emax >= ec)) {
-    int32_t sc = 0;                                      // line 7: RD to c_frac (= F_p) bits
-    if (cS) {
-      const int32_t v = cneg ? -(int32_t)cS : (int32_t)cS;
-      const int32_t sh = emax - ec + 23 - m.c_frac;
-      sc = sh >= 0 ? sar32(v, sh) : v * (1 << (-sh));
-    }
-    const int32_t Sacc = Sp + sc;                       // line 8
-    if (Sacc == 0) {                                     // a nonzero product cancelled: +0
-      r = 0u;
-      return true;
-    }
-    return hw_round32_1(Sacc, emax - m.F, m.rne, r);      // line 15
-  }
-  // line 10: S_p on c's grid with RD (floor) at psum_frac fraction bits; in this branch
-  // e_max < e_c, so the shift is at least 1 - (psum_frac - F_p) >= -8 and the product
-  // sum, pre-shifted by 16, is floored by one arithmetic shift
-  int64_t Sacc = have_p ? (((int64_t)Sp << 16) >> min(ec - emax - (m.psum_frac - m.F) + 16, 63)) : 0;
-  const int64_t vc = cneg ? -(int64_t)cS : (int64_t)cS;
-  Sacc += vc * ((int64_t)1 << (m.psum_frac - 23));       // line 11
-  if (Sacc == 0) {
-    r = 0u;
-    return have_p || cS != 0u;
-  }
-  // lines 12-13: normalise (exponent floored at -126) and RD to post_norm_frac bits.
-  // The leading bit of |S| is found from S xor its sign: one place lower only when
-  // |S| is a power of two, where every lower bit is zero and the RD is exact anyway.
-  int32_t lsb = ec - m.psum_frac;
-  const int32_t p = 63 - __clzll((long long)(Sacc ^ (Sacc >> 63)));
-  const int32_t rsh = max(p + lsb, -126) - m.post_norm_frac - lsb;
-  if (rsh > 0) {
-    Sacc >>= min(rsh, 63);                               // floor = RD for either sign
-    lsb += rsh;
-  }
-  return hw_round64_1(Sacc, lsb, m.rne, r);                // line 15
-}
-
 // A NaN pattern no model returns (their NaN results are always nan_bits): it marks
 // an output the fast kernel left to the general evaluator.
 __host__ __device__ __forceinline__ uint32_t redo_mark(const DevModel &m) {
   return m.nan_bits == 0x7FFFFFFFu ? 0xFFFFFFFFu : 0x7FFFFFFFu;
 }
 
-// C == nullptr stands for C = 0.
+// Both kernels below: C == nullptr stands for C = 0.
 //
 // SPARSE = 1: A is given 2:4-compressed (Ac [M][K/2], meta [M][K/4]) and is expanded
 // into the dense panel while staging; kt and K are then dense sizes and a block spans
@@ -207,8 +150,206 @@ __host__ __device__ __forceinline__ uint32_t redo_mark(const DevModel &m) {
 // nothing to the aligned sum: the result is the compressed chain's.  The cases where
 // that argument needs finite operands, a nonzero sum or valid metadata (idx0 < idx1)
 // are the ones sent to the general evaluator of the compressed chain.
-template <int ARCH, int ESZ, int SPARSE>
-__global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_constant__ DevModel m, int kt, int kblk,
+//
+// Early-c global alignment (Table 3's early-c model) with the accumulator carried
+// between blocks as f * 2^g: f is the block result's rounded significand as an
+// integer-valued float (|f| < 2^31, or the addend's 24-bit significand before the
+// first block) and g its scale.  Per block:
+//  - e_c = max(floor(log2 |f|) + g, -126), read from f's exponent field (the -126
+//    floor gives a subnormal addend the exponent e_min, as the decoder does);
+//  - the aligned addend trunc(c * 2^(F_p - e_max)) = trunc(f * 2^(g + F_p - e_max)) is
+//    one exact multiply by a power of two and one conversion with truncation toward
+//    zero (RZ on the magnitude, the model's truncation); a scale below 2^-126 stands
+//    for 0, which is the truncated value there since |f| < 2^31;
+//  - the rounding of the sum S to 24 bits is the int->fp32 conversion (RNE or RZ,
+//    RM), and the new scale is e_max - F_p.
+// This equals rounding S * 2^(e_max - F_p) to fp32 while the result is normal; each
+// thread tracks the exponent range of its results, and a result above 2^127 or below
+// 2^-126 (overflow, subnormal) sends the thread's outputs to the fixup pass, as do
+// Inf/NaN operands, a zero sum of zero terms and a possible CDNA 3 product overflow.
+template <int ESZ, int SPARSE, int RM>
+__global__ void __launch_bounds__(kFThreads, 2) gemm_early_kernel(const __grid_constant__ DevModel m, int kt, int kblk,
+                                                                int M, int N, int K, const uint8_t *__restrict__ A,
+                                                                int64_t lda, const uint8_t *__restrict__ meta,
+                                                                int64_t ldm, const uint8_t *__restrict__ Bt,
+                                                                int64_t ldb, const uint32_t *C, int64_t ldc,
+                                                                uint32_t *D, int64_t ldd) {
+  extern __shared__ int32_t fsm[];
+  const int KC = fast_chunk(kt);
+  int32_t *aS = fsm, *aE = aS + KC * kFS, *aG = aE + KC * kFS;         // [KC][kFS]
+  int32_t *bS = aG + KC * kFS, *bE = bS + KC * kFS, *bG = bE + KC * kFS;  // B significands << P0
+  uint8_t *aSpec = reinterpret_cast<uint8_t *>(bG + KC * kFS);          // [kFB] per row
+  uint8_t *bSpec = aSpec + kFB;
+  const int i0 = blockIdx.y * kFB, j0 = blockIdx.x * kFB;
+  const int tid = threadIdx.x;
+  const int ti = (tid / (kFB / kFT)) * kFT, tj = (tid % (kFB / kFT)) * kFT;
+  const int32_t F = m.F;
+  // a zero sum is +0 when some term is nonzero; that is e_max > -1024 only when
+  // neither a c = 0 exponent nor an exponent limit can raise e_max
+  const bool nz_by_emax = m.c_zero_exp <= -1024 && m.emin_lim <= -1024;
+
+  float fv[kFT][kFT];                    // accumulator: fv * 2^(gq + 127 - ...) (see above)
+  int32_t gq[kFT][kFT];                  // g - 127
+  int32_t raw[kFT][kFT];                 // floor(log2 |f|) + g, the accumulator's exponent
+  uint32_t redo = 0;                     // outputs to recompute with the general evaluator
+  int32_t lo = 0, hi = 0;                // exponent range of this thread's block results
+#pragma unroll
+  for (int a = 0; a < kFT; a++)
+#pragma unroll
+    for (int b = 0; b < kFT; b++) {
+      const int i = i0 + ti + a, j = j0 + tj + b;
+      const uint32_t cb = (C && i < M && j < N) ? C[(int64_t)i * ldc + j] : 0u;
+      uint32_t cS, cneg;
+      int32_t cE;
+      decode_c(m, cb, cS, cE, cneg);
+      if ((cb & 0x7F800000u) == 0x7F800000u) {
+        redo |= 1u << (a * kFT + b);
+        cS = 0u;
+      }
+      fv[a][b] = cneg ? -(float)cS : (float)cS;
+      gq[a][b] = cE - 23 - 127;
+      raw[a][b] = cE;                     // e_c of a nonzero c (-126 when subnormal)
+    }
+
+  for (int k0 = 0; k0 < K; k0 += KC) {
+    const int kc = min(KC, K - k0);
+    __syncthreads();
+    if (tid < kFB) { aSpec[tid] = 0; bSpec[tid] = 0; }
+    __syncthreads();
+    stage_chunk<ESZ, SPARSE>(m, m.P0, i0, j0, k0, kc, KC, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, bS, bE, bG,
+                             aSpec, bSpec);
+    __syncthreads();
+    // an Inf/NaN in a row of A or a column of B (or invalid metadata) sends the whole
+    // row / column of this thread's tile to the fixup pass
+#pragma unroll
+    for (int a = 0; a < kFT; a++)
+      if (aSpec[ti + a]) redo |= 0xFu << (a * kFT);
+#pragma unroll
+    for (int b = 0; b < kFT; b++)
+      if (bSpec[tj + b]) redo |= 0x1111u << b;
+
+    for (int s0 = 0; s0 < kc; s0 += kt) {
+      const int send = min(s0 + kt, kc);
+      for (int b0 = s0; b0 < send; b0 += kblk) {
+        const int nt = min(kblk, send - b0);
+        // ---- e_max: c's exponent and the limit first, then the products
+        int32_t em[kFT][kFT];
+#pragma unroll
+        for (int a = 0; a < kFT; a++)
+#pragma unroll
+          for (int b = 0; b < kFT; b++) {
+            const int32_t ec = fv[a][b] == 0.0f ? m.c_zero_exp : max(raw[a][b], -126);
+            em[a][b] = max(ec, m.emin_lim);
+          }
+        for (int q = b0; q < b0 + nt; q++) {
+          const int4 ea = *reinterpret_cast<const int4 *>(aE + q * kFS + ti);
+          const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
+          const int32_t xa[4] = {ea.x, ea.y, ea.z, ea.w}, xb[4] = {eb.x, eb.y, eb.z, eb.w};
+#pragma unroll
+          for (int a = 0; a < kFT; a++)
+#pragma unroll
+            for (int b = 0; b < kFT; b++) em[a][b] = __viaddmax_s32(xa[a], xb[b], em[a][b]);
+        }
+        // ---- the aligned addend starts the sum
+        int32_t Sp[kFT][kFT];
+#pragma unroll
+        for (int a = 0; a < kFT; a++)
+#pragma unroll
+          for (int b = 0; b < kFT; b++) {
+            // 2^(g + F - e_max) as a float: exponent field g + F - e_max + 127, 0 below 2^-126
+            const int32_t se = max(gq[a][b] + 254 + F - em[a][b], 0);
+            const float sc = __fmul_rz(fv[a][b], __uint_as_float((uint32_t)se << 23));
+            Sp[a][b] = fv[a][b] == 0.0f ? 0 : __float2int_rz(sc);
+          }
+        // ---- aligned, truncated products
+        for (int q = b0; q < b0 + nt; q++) {
+          const int4 sa = *reinterpret_cast<const int4 *>(aS + q * kFS + ti);
+          const int4 ea = *reinterpret_cast<const int4 *>(aE + q * kFS + ti);
+          const int4 ga = *reinterpret_cast<const int4 *>(aG + q * kFS + ti);
+          const int4 sb = *reinterpret_cast<const int4 *>(bS + q * kFS + tj);
+          const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
+          const int4 gb = *reinterpret_cast<const int4 *>(bG + q * kFS + tj);
+          const int32_t SA[4] = {sa.x, sa.y, sa.z, sa.w}, EA[4] = {ea.x, ea.y, ea.z, ea.w}, GA[4] = {ga.x, ga.y, ga.z, ga.w};
+          const int32_t SB[4] = {sb.x, sb.y, sb.z, sb.w}, EB[4] = {eb.x, eb.y, eb.z, eb.w}, GB[4] = {gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+          for (int a = 0; a < kFT; a++)
+#pragma unroll
+            for (int b = 0; b < kFT; b++) {
+              const int32_t sh = em[a][b] + m.R0 - EA[a] - EB[b];
+              const uint32_t U = (uint32_t)(SA[a] * SB[b]);
+              const int32_t t = (int32_t)shr32(U, sh);
+              Sp[a][b] += t * (GA[a] * GB[b]);
+            }
+        }
+        // ---- round: the new accumulator and its exponent
+#pragma unroll
+        for (int a = 0; a < kFT; a++)
+#pragma unroll
+          for (int b = 0; b < kFT; b++) {
+            const int32_t S = Sp[a][b];
+            const float f = RM ? __int2float_rn(S) : __int2float_rz(S);
+            const int32_t g = em[a][b] - F;
+            int32_t r = (int32_t)((__float_as_uint(f) >> 23) & 0xFFu) + g - 127;
+            if (S == 0) {
+              r = 0;
+              if (!(nz_by_emax && em[a][b] > -1024)) redo |= 1u << (a * kFT + b);
+            }
+            lo = min(lo, r);
+            hi = max(hi, r);
+            fv[a][b] = f;
+            gq[a][b] = g - 127;
+            raw[a][b] = r;
+            if (m.prod_ovf && em[a][b] >= 126) redo |= 1u << (a * kFT + b);
+          }
+      }
+    }
+  }
+  // a result outside the normal range anywhere in this thread's chains: all its
+  // outputs take the fixup pass (gemm_fixup_kernel; C does not alias D here)
+  if (lo < -126 || hi > 127) redo = 0xFFFFu;
+#pragma unroll
+  for (int a = 0; a < kFT; a++)
+#pragma unroll
+    for (int b = 0; b < kFT; b++) {
+      const int i = i0 + ti + a, j = j0 + tj + b;
+      if (i >= M || j >= N) continue;
+      uint32_t r;
+      if (K == 0) {
+        r = C ? C[(int64_t)i * ldc + j] : 0u;
+      } else if ((redo >> (a * kFT + b)) & 1u) {
+        r = redo_mark(m);
+      } else {
+        // f * 2^g is a normal float (or f = 0): the two scalings are exact
+        const int32_t g = gq[a][b] + 127;
+        const int32_t k1 = min(max(g, -96), 96), k2 = g - k1;
+        const float y = __fmul_rn(__fmul_rn(fv[a][b], __uint_as_float((uint32_t)(k1 + 127) << 23)),
+                                  __uint_as_float((uint32_t)(k2 + 127) << 23));
+        r = fv[a][b] == 0.0f ? 0u : __float_as_uint(y);
+      }
+      D[(int64_t)i * ldd + j] = r;
+    }
+}
+
+// Algorithm 1 (late c) with the accumulator carried as f * 2^g (as in
+// gemm_early_kernel) and both branches of the merge (lines 6-14) in one branch-free
+// sequence.  With d = e_c - e_max and s = max(d - (psum_frac - F_p), 0), the sum is
+// formed in units of 2^(e_max - F_p + s): the units of the product sum S_p while c's
+// grid of psum_frac fraction bits (line 10) is no coarser than S_p's, else c's grid.
+//  - X = floor(c * 2^-(e_max - F_p + s)) is c aligned to c_frac = F_p fraction bits and
+//    rounded down (line 7) when d <= 0, and c exactly when d > 0 (line 11: c's grid
+//    2^(e_c - 23) is then no finer than the units); |X| < 2^(psum_frac + 1).  One exact
+//    multiply by a power of two and one conversion rounding down;
+//  - floor(S_p / 2^s) is line 10's round-down of S_p onto c's grid (s = 0: exact);
+//  - T = floor(S_p / 2^s) + X is then the sum of line 8 (d <= 0) or that of line 11
+//    (d > 0) up to a power of two; for d > 0 lines 12-13 floor T to post_norm_frac + 1
+//    significant bits, which in two's complement clears the low bits;
+//  - line 15 is the int64 -> fp32 conversion, and g becomes e_max - F_p + s.
+// The normalisation's exponent floor at -126 and the fp32 range are handled as in
+// gemm_early_kernel: a result outside the normal range sends the thread's outputs to
+// the fixup pass.  A block without products leaves the accumulator as it is (lines
+// 11-15 reproduce c), or goes to the fixup pass when c = 0 too.
+template <int ESZ, int SPARSE, int RM>
+__global__ void __launch_bounds__(kFThreads, 2) gemm_late_kernel(const __grid_constant__ DevModel m, int kt, int kblk,
                                                                int M, int N, int K, const uint8_t *__restrict__ A,
                                                                int64_t lda, const uint8_t *__restrict__ meta,
                                                                int64_t ldm, const uint8_t *__restrict__ Bt,
@@ -223,17 +364,30 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
   const int i0 = blockIdx.y * kFB, j0 = blockIdx.x * kFB;
   const int tid = threadIdx.x;
   const int ti = (tid / (kFB / kFT)) * kFT, tj = (tid % (kFB / kFT)) * kFT;
+  const int32_t F = m.F;
+  const int32_t dpsum = m.psum_frac - F;              // line 10 floors S_p only beyond this gap
 
-  uint32_t acc[kFT][kFT];
+  float fv[kFT][kFT];                    // accumulator significand (integer-valued)
+  int32_t gs[kFT][kFT];                  // its scale g
+  uint32_t redo = 0;
+  int32_t lo = 0, hi = 0;                // exponent range of this thread's block results
 #pragma unroll
   for (int a = 0; a < kFT; a++)
 #pragma unroll
     for (int b = 0; b < kFT; b++) {
       const int i = i0 + ti + a, j = j0 + tj + b;
-      acc[a][b] = (C && i < M && j < N) ? C[(int64_t)i * ldc + j] : 0u;
+      const uint32_t cb = (C && i < M && j < N) ? C[(int64_t)i * ldc + j] : 0u;
+      uint32_t cS, cneg;
+      int32_t cE;
+      decode_c(m, cb, cS, cE, cneg);
+      if ((cb & 0x7F800000u) == 0x7F800000u) {
+        redo |= 1u << (a * kFT + b);
+        cS = 0u;
+      }
+      fv[a][b] = cneg ? -(float)cS : (float)cS;
+      gs[a][b] = cE - 23;
     }
 
-  uint32_t redo = 0;                     // outputs to recompute with the general evaluator
   for (int k0 = 0; k0 < K; k0 += KC) {
     const int kc = min(KC, K - k0);
     __syncthreads();
@@ -242,22 +396,23 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
     stage_chunk<ESZ, SPARSE>(m, m.P0, i0, j0, k0, kc, KC, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, bS, bE, bG,
                              aSpec, bSpec);
     __syncthreads();
-    uint32_t rowsp = 0, colsp = 0;
 #pragma unroll
-    for (int a = 0; a < kFT; a++) rowsp |= (uint32_t)aSpec[ti + a] << a;
+    for (int a = 0; a < kFT; a++)
+      if (aSpec[ti + a]) redo |= 0xFu << (a * kFT);
 #pragma unroll
-    for (int b = 0; b < kFT; b++) colsp |= (uint32_t)bSpec[tj + b] << b;
+    for (int b = 0; b < kFT; b++)
+      if (bSpec[tj + b]) redo |= 0x1111u << b;
 
     for (int s0 = 0; s0 < kc; s0 += kt) {
       const int send = min(s0 + kt, kc);
       for (int b0 = s0; b0 < send; b0 += kblk) {
         const int nt = min(kblk, send - b0);
-        // ---- pass 1: e_max of the products (c joins for the early-c model)
-        int32_t emax[kFT][kFT];
+        // ---- e_max of the products (line 3)
+        int32_t em[kFT][kFT];
 #pragma unroll
         for (int a = 0; a < kFT; a++)
 #pragma unroll
-          for (int b = 0; b < kFT; b++) emax[a][b] = kNegE;
+          for (int b = 0; b < kFT; b++) em[a][b] = kNegE;
         for (int q = b0; q < b0 + nt; q++) {
           const int4 ea = *reinterpret_cast<const int4 *>(aE + q * kFS + ti);
           const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
@@ -265,33 +420,14 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
 #pragma unroll
           for (int a = 0; a < kFT; a++)
 #pragma unroll
-            for (int b = 0; b < kFT; b++) emax[a][b] = __viaddmax_s32(xa[a], xb[b], emax[a][b]);
+            for (int b = 0; b < kFT; b++) em[a][b] = __viaddmax_s32(xa[a], xb[b], em[a][b]);
         }
-        uint32_t hpm = 0;
-        // ---- c's exponent (early c) and the shift base
-        int32_t base[kFT][kFT];
+        // ---- aligned, truncated products (line 4)
         int32_t Sp[kFT][kFT];
 #pragma unroll
         for (int a = 0; a < kFT; a++)
 #pragma unroll
-          for (int b = 0; b < kFT; b++) {
-            int32_t em = emax[a][b];
-            Sp[a][b] = 0;
-            if constexpr (ARCH == MCEMU_ARCH_GA_EARLY) {
-              // c joins e_max and is aligned here, so the sum starts with its term
-              uint32_t cS, cneg;
-              int32_t cE;
-              decode_c(m, acc[a][b], cS, cE, cneg);
-              const int32_t ec = cS ? cE : m.c_zero_exp;
-              em = max(max(em, ec), m.emin_lim);
-              if (emax[a][b] > -1024 || cS) hpm |= 1u << (a * kFT + b);   // a nonzero term
-              emax[a][b] = em;
-              if (cS)                                     // truncation (the kernel takes no RD model)
-                Sp[a][b] = (int32_t)shr32(cS * m.p0cmul, em + m.R0c - cE) * (1 - 2 * (int32_t)cneg);
-            }
-            base[a][b] = em + m.R0;
-          }
-        // ---- pass 2: aligned, truncated products
+          for (int b = 0; b < kFT; b++) Sp[a][b] = 0;
         for (int q = b0; q < b0 + nt; q++) {
           const int4 sa = *reinterpret_cast<const int4 *>(aS + q * kFS + ti);
           const int4 ea = *reinterpret_cast<const int4 *>(aE + q * kFS + ti);
@@ -305,41 +441,71 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_fast_kernel(const __grid_co
           for (int a = 0; a < kFT; a++)
 #pragma unroll
             for (int b = 0; b < kFT; b++) {
-              const int32_t sh = base[a][b] - EA[a] - EB[b];
+              const int32_t sh = em[a][b] + m.R0 - EA[a] - EB[b];
               const uint32_t U = (uint32_t)(SA[a] * SB[b]);
               const int32_t t = (int32_t)shr32(U, sh);
               Sp[a][b] += t * (GA[a] * GB[b]);
             }
         }
-        // ---- merge with c and round; outputs that leave the fast path are redone
+        // ---- the merge with c (lines 5-15)
 #pragma unroll
         for (int a = 0; a < kFT; a++)
 #pragma unroll
           for (int b = 0; b < kFT; b++) {
-            const uint32_t cb = acc[a][b];
-            uint32_t r = 0;
-            bool ok = !((((rowsp >> a) | (colsp >> b)) & 1u) || (cb & 0x7F800000u) == 0x7F800000u ||
-                        (m.prod_ovf && emax[a][b] >= 126));
-            if (ok) {
-              if constexpr (ARCH == MCEMU_ARCH_GA_EARLY)
-                ok = merge_early(m, Sp[a][b], emax[a][b], (hpm >> (a * kFT + b)) & 1u, r);
-              else ok = merge_late(m, Sp[a][b], emax[a][b], cb, r);
+            const int32_t e = em[a][b];
+            // e_c = floor(log2 |c|), no lower than -126 (a subnormal addend), from f's
+            // exponent field; c_zero_exp for c = 0
+            const int32_t ecv = fv[a][b] == 0.0f ? m.c_zero_exp
+                                : max((int32_t)((__float_as_uint(fv[a][b]) >> 23) & 0xFFu) + gs[a][b] - 127, -126);
+            const int32_t d = ecv - e;
+            const bool have_p = e > -1024;                 // zero products sit below -1700
+            const int32_t sg = max(d - dpsum, 0);
+            const int32_t u = e - F + sg;                  // the units' exponent
+            // X: 2^(g - u) as a float, no lower than 2^-126 (|f| * 2^-126 < 1 floors
+            // like any smaller positive or negative value)
+            const int32_t se = max(gs[a][b] + 127 - u, 1);
+            const int64_t X = fv[a][b] == 0.0f ? 0ll
+                              : __float2ll_rd(__fmul_rn(fv[a][b], __uint_as_float((uint32_t)se << 23)));
+            int64_t T = (int64_t)(Sp[a][b] >> min(sg, 31)) + X;
+            const int32_t p = 63 - __clzll((long long)(T ^ (T >> 63)));
+            const int32_t rsh = d > 0 ? max(p - m.post_norm_frac, 0) : 0;
+            T = (T >> rsh) << rsh;
+            const float f = RM ? __ll2float_rn(T) : __ll2float_rz(T);
+            int32_t r = (int32_t)((__float_as_uint(f) >> 23) & 0xFFu) + u - 127;
+            if (T == 0) r = 0;
+            if (have_p) {
+              lo = min(lo, r);
+              hi = max(hi, r);
+              fv[a][b] = f;
+              gs[a][b] = u;
+              if (m.prod_ovf && e >= 126) redo |= 1u << (a * kFT + b);
+            } else if (fv[a][b] == 0.0f) {
+              redo |= 1u << (a * kFT + b);               // no product and c = 0
             }
-            if (!ok) redo |= 1u << (a * kFT + b);
-            acc[a][b] = r;
           }
       }
     }
   }
-  // flagged outputs get the mark; gemm_fixup_kernel recomputes them afterwards (C
-  // does not alias D on this path).  Keeping the general evaluator out of this kernel
-  // keeps its register allocation free of a call.
+  if (lo < -126 || hi > 127) redo = 0xFFFFu;
 #pragma unroll
   for (int a = 0; a < kFT; a++)
 #pragma unroll
     for (int b = 0; b < kFT; b++) {
       const int i = i0 + ti + a, j = j0 + tj + b;
-      if (i < M && j < N) D[(int64_t)i * ldd + j] = ((redo >> (a * kFT + b)) & 1u) ? redo_mark(m) : acc[a][b];
+      if (i >= M || j >= N) continue;
+      uint32_t r;
+      if (K == 0) {
+        r = C ? C[(int64_t)i * ldc + j] : 0u;
+      } else if ((redo >> (a * kFT + b)) & 1u) {
+        r = redo_mark(m);
+      } else {
+        const int32_t g = gs[a][b];
+        const int32_t k1 = min(max(g, -96), 96), k2 = g - k1;
+        const float y = __fmul_rn(__fmul_rn(fv[a][b], __uint_as_float((uint32_t)(k1 + 127) << 23)),
+                                  __uint_as_float((uint32_t)(k2 + 127) << 23));
+        r = fv[a][b] == 0.0f ? 0u : __float_as_uint(y);
+      }
+      D[(int64_t)i * ldd + j] = r;
     }
 }
 
@@ -375,7 +541,8 @@ static int run_fast(const DevModel &m, int kt, int M, int N, int K, const void *
                     int64_t ldb, const uint32_t *C, int64_t ldc, uint32_t *D, int64_t ldd, cudaStream_t s,
                     const uint8_t *meta = nullptr, int64_t ldm = 0) {
   const size_t shm = (size_t)6 * fast_chunk(kt) * kFS * 4 + 2 * kFB;
-  auto kern = gemm_fast_kernel<ARCH, ESZ, SPARSE>;
+  auto kern = ARCH == MCEMU_ARCH_GA_EARLY ? (m.rne ? gemm_early_kernel<ESZ, SPARSE, 1> : gemm_early_kernel<ESZ, SPARSE, 0>)
+                                          : (m.rne ? gemm_late_kernel<ESZ, SPARSE, 1> : gemm_late_kernel<ESZ, SPARSE, 0>);
   if (shm > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm) != cudaSuccess)
     return MCEMU_ERR_UNSUPPORTED;

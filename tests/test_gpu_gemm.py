@@ -86,6 +86,55 @@ def test_tile_gemm_full(L, case, shape):
     assert len(bad) == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
 
 
+EARLY_RANGE_CASES = [  # format, element scale 2^s, addend scale 2^t, model options
+    ("bf16", -63, -126, dict(out_round="rne")),                       # results cross into subnormals
+    ("bf16", -63, -130, dict(out_round="rtz", sub_in_flush=True)),
+    ("bf16", 62, 123, dict(out_round="rne")),                         # results overflow mid-chain
+    ("bf16", 62, 125, dict(out_round="rtz")),
+    ("bf16", 0, 0, dict(out_round="rne", emin_lim=-133, c_zero_exp=-126)),
+    ("fp16", None, None, dict(out_round="rne")),                      # random bit patterns
+    ("fp16", -7, -140, dict(out_round="rtz", align_frac=20)),
+    ("e4m3", None, None, dict(out_round="rtz", n_fma=8)),
+    ("e5m2", -8, -135, dict(out_round="rne", n_fma=8, align_frac=29)),
+    ("xf32", 40, 100, dict(out_round="rne", n_fma=2, align_frac=24)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(EARLY_RANGE_CASES)))
+def test_early_c_gemm_exponent_ranges(L, case):
+    """Early-c global alignment through the fast GEMM kernel with chains whose partial
+    results leave the normal fp32 range (overflow, subnormal), subnormal and zero
+    addends, exponent limits and flushed inputs, over several CTA tiles with ragged
+    edges: every output against the oracle."""
+    fmt, s, t, opts = EARLY_RANGE_CASES[case]
+    spec = dict(dict(fmt_a=fmt, fmt_b=fmt, arch="ga_early", n_fma=4, align_frac=26), **opts)
+    rng = np.random.default_rng(40 + case)
+    M, N, K, kt = 70, 67, 200, 2 * spec["n_fma"]
+    if s is None:
+        A = W.independent_bits(rng, fmt, (M, K), "ocp", 0.0)
+        Bt = W.independent_bits(rng, fmt, (N, K), "ocp", 0.0)
+        C = W.independent_bits(rng, "fp32", (M, N), "ocp", 0.0)
+    else:
+        def draw(shape):
+            x = rng.standard_normal(shape) * 2.0 ** s
+            x[rng.random(shape) < 0.05] = 0.0
+            if fmt == "bf16":
+                return W.fp32_to_bf16_rne(x.astype(np.float32))
+            if fmt == "xf32":
+                return x.astype(np.float32).view(np.uint32) & np.uint32(0xFFFFE000)
+            return W.nearest_even(x, fmt)
+        A, Bt = draw((M, K)), draw((N, K))
+        c = (rng.standard_normal((M, N)) * 2.0 ** t).astype(np.float32)
+        c[rng.random((M, N)) < 0.1] = 0.0
+        C = c.view(np.uint32).copy()
+    m = L.Model(spec)
+    D = host_u32(L.tile_gemm(m, L.tile(0, 16, 16, kt, 4), dev(A), dev(Bt), dev(C)))
+    ii, jj = all_entries(M, N)
+    want = oracle.gemm_entries(spec, K, kt, A, Bt, C, ii, jj).reshape(M, N)
+    bad = np.argwhere(D != want)
+    assert len(bad) == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
+
+
 def test_tile_gemm_specials_and_zero_k(L):
     spec = PRESETS["cdna3_bf16"]
     A, Bt, C = operands("bf16", 20, 20, 64, seed=5, special_rate=0.03)
