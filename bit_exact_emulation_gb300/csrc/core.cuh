@@ -1115,6 +1115,61 @@ __device__ __forceinline__ uint32_t block_fma_fast(const DevModel &m, const uint
   return block_fma_terms<ARCH, ID, K, UT, AT, RM>(m, p, cbits, spec, slow);
 }
 
+// ---------------------------------------------------------------------------
+// EXACT on the FP32 pipe, for operands whose products fp32 holds exactly and
+// whose sum with an fp32 c cannot overflow (FP16: |p| < 2^32 and >= 2^-48 when
+// nonzero; FP8 likewise).  Error-free transformations (Knuth's TwoSum) carry the
+// exact sum S = c + p_1 + ... + p_K as s + e_1 + ... + e_K; E' = fl(sum e_l) is off
+// from the exact error sum by at most gamma_(K-1) * sum |e_l| (Higham, Accuracy and
+// Stability of Numerical Algorithms, Sec. 4.2), bounded above by b with upward
+// rounding; then TwoSum(s, E') = t + r exactly, so S = t + r + d with |d| <= b.
+// t = RN(s + E') is RN(S) when |r| + b < ulp(t)/2 (or b = 0: S = t + r exactly, and
+// the hardware's RNE of that sum is t); RZ(S) is t when sign(t) r >= b and the
+// neighbour of t toward zero when sign(t) r < -b, given b < ulp(t)/4.  Everything
+// else (a result below 2^-124, an undecided rounding) is left to the integer path.
+// Returns 0 with out set, 1 when the IEEE sum is not finite (an Inf or NaN operand),
+// 2 when the rounding is not decided here.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fadd_rn(s, -a);
+  e = __fadd_rn(__fadd_rn(a, -__fadd_rn(s, -bb)), __fadd_rn(b, -bb));
+}
+
+template <int K>
+__device__ __forceinline__ int exact_fp32_sum(const float (&p)[K], uint32_t cbits, int rne, uint32_t &out) {
+  float s = __uint_as_float(cbits), e[K];
+#pragma unroll
+  for (int l = 0; l < K; l++) two_sum(s, p[l], s, e[l]);
+  float E = e[0], a = fabsf(e[0]);
+#pragma unroll
+  for (int l = 1; l < K; l++) {
+    E = __fadd_rn(E, e[l]);
+    a = __fadd_ru(a, fabsf(e[l]));
+  }
+  // gamma_(K-1) = (K-1) u / (1 - (K-1) u) < (K-1) 2^-23.9 <= 2^(ceil(log2(K-1)) - 23)
+  constexpr float kGamma = K <= 2 ? 0x1p-23f : K <= 3 ? 0x1p-22f : K <= 5 ? 0x1p-21f : K <= 9 ? 0x1p-20f
+                                                     : K <= 17 ? 0x1p-19f : 0x1p-18f;
+  const float b = __fmul_ru(a, kGamma);
+  float t, r;
+  two_sum(s, E, t, r);
+  const uint32_t tb = __float_as_uint(t), ef = tb & 0x7F800000u;
+  if (ef == 0x7F800000u) return 1;
+  if (ef < (3u << 23)) return 2;                       // |t| < 2^-124: zero, subnormal, near them
+  const float pt = __uint_as_float(ef);                // 2^e_t
+  if (rne) {
+    if (b == 0.0f || ((tb & 0x7FFFFFu) != 0u && __fadd_ru(fabsf(r), b) < __fmul_rn(pt, 0x1p-24f))) {
+      out = tb;
+      return 0;
+    }
+    return 2;
+  }
+  if (b >= __fmul_rn(pt, 0x1p-25f)) return 2;
+  const float sr = (tb >> 31) ? -r : r;                // r measured away from zero
+  if (sr >= b) { out = tb; return 0; }
+  if (-sr > b) { out = tb - 1u; return 0; }            // the neighbour of t toward zero
+  return 2;
+}
+
 // Powers of two (and 2^22 - 1) for fterms_w16, passed in at run time so that the
 // compiler keeps them as multiplies (FMA pipe) instead of shifts and masks (ALU).
 struct W16Consts {

@@ -147,6 +147,8 @@ __global__ void __launch_bounds__(kStreamThreads) fast_kernel(const __grid_const
   constexpr int NB = KM * Fmt<ID>::BYTES;
   constexpr int NW = (NB + 3) / 4;
   constexpr bool kWords = Fmt<ID>::BYTES == 2 && Fmt<ID>::XF == 0;   // packed 16-bit decode
+  // exact-then-round of FP16 sets on the FP32 pipe first (exact_fp32_sum)
+  constexpr bool kFp32Exact = ARCH == MCEMU_ARCH_EXACT && ID == F_FP16;
   constexpr bool kDefer = ARCH == MCEMU_ARCH_EXACT && (ID == F_FP16 || ID == F_BF16 || ID == F_XF32T ||
                                                        ID == F_XF32R);
   __shared__ size_t queue[kStreamThreads / 32][64];
@@ -177,7 +179,21 @@ __global__ void __launch_bounds__(kStreamThreads) fast_kernel(const __grid_const
       nc = __ldcs(c + vn);
     }
     bool special = false, slow = false;
-    if (v < n) {
+    if (kFp32Exact && v < n) {
+      float p[KM];
+#pragma unroll
+      for (int i = 0; i < KM / 2; i++) {
+        const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&wa[i]));
+        const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&wb[i]));
+        p[2 * i] = __fmul_rn(fa.x, fb.x);
+        p[2 * i + 1] = __fmul_rn(fa.y, fb.y);
+      }
+      uint32_t r = 0u;
+      const int st = exact_fp32_sum<KM>(p, cb, out_rne<RM>(m), r);
+      special = st == 1;
+      slow = st == 2;
+      if (st == 0) __stcs(d + v, r);
+    } else if (v < n) {
       uint32_t sw = (cb & 0x7F800000u) == 0x7F800000u;
 #pragma unroll
       for (int i = 0; i < NW; i++) sw |= fspecial_word<ID>(wa[i]) | fspecial_word<ID>(wb[i]);

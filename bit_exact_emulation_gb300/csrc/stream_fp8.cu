@@ -244,6 +244,66 @@ __device__ __forceinline__ uint32_t f8_exact(const DevModel &m, const uint32_t (
   return exact_fixed_merge<ID>(m, W << 39, cS, cE, cneg, cb);
 }
 
+// One vector set through the product table: specials, then the model.
+template <int ARCH, int ID, int K, bool RNE>
+__device__ __forceinline__ uint32_t f8_eval(const DevModel &m, const PipeConsts &pc, const uint16_t *tab,
+                                            const uint32_t (&wa)[K / 4], const uint32_t (&wb)[K / 4], uint32_t cb) {
+  constexpr int NW = K / 4;
+  uint32_t e[K], sg[K];
+  f8_lookup<K>(tab, wa, wb, e, sg);
+  uint32_t mx = 0, orv = 0;
+#pragma unroll
+  for (int l = 0; l < K; l++) {
+    mx = max(mx, e[l]);
+    orv |= e[l];
+  }
+  uint32_t fnuz_nan = 0;
+  if constexpr (Fmt<ID>::FNUZ) {
+#pragma unroll
+    for (int w = 0; w < NW; w++) fnuz_nan |= fspecial_word<ID>(wa[w]) | fspecial_word<ID>(wb[w]);
+  }
+  if ((orv & 0x300u) || (cb & 0x7F800000u) == 0x7F800000u || fnuz_nan)
+    return f8_special<ID, K>(m, e, sg, orv, cb, fnuz_nan);
+  if constexpr (ARCH == MCEMU_ARCH_GA_EARLY) return f8_ga_early<ID, K, RNE>(m, pc, e, sg, cb, mx);
+  else return f8_exact<ID, K>(m, e, sg, cb, mx);
+}
+
+template <int K>
+__device__ __forceinline__ void f8_load(const uint8_t *__restrict__ a, const uint8_t *__restrict__ b,
+                                        const uint32_t *__restrict__ c, size_t u, uint32_t (&wa)[K / 4],
+                                        uint32_t (&wb)[K / 4], uint32_t &cb) {
+#pragma unroll
+  for (int w = 0; w < K / 4; w += 2) {
+    const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(a + u * K) + w / 2);
+    const uint2 y = __ldcs(reinterpret_cast<const uint2 *>(b + u * K) + w / 2);
+    wa[w] = x.x; wa[w + 1] = x.y;
+    wb[w] = y.x; wb[w + 1] = y.y;
+  }
+  cb = __ldcs(c + u);
+}
+
+// Exact-then-round of one OCP FP8 set on the FP32 pipe (exact_fp32_sum): FP8 -> f16
+// -> f32 is exact, and so are the products.  False when the set has an Inf/NaN
+// operand or addend or the rounding is not decided there.
+template <int ID, int K>
+__device__ __forceinline__ bool f8_exact_fp32(const DevModel &m, const uint32_t (&wa)[K / 4],
+                                              const uint32_t (&wb)[K / 4], uint32_t cb, uint32_t &r) {
+  float p[K];
+  constexpr __nv_fp8_interpretation_t kind = ID == F_E4M3 ? __NV_E4M3 : __NV_E5M2;
+#pragma unroll
+  for (int w = 0; w < K / 4; w++)
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+      const float2 fa = __half22float2(__half2(
+          __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(wa[w] >> (16 * h)), kind)));
+      const float2 fb = __half22float2(__half2(
+          __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(wb[w] >> (16 * h)), kind)));
+      p[4 * w + 2 * h] = __fmul_rn(fa.x, fb.x);
+      p[4 * w + 2 * h + 1] = __fmul_rn(fa.y, fb.y);
+    }
+  return exact_fp32_sum<K>(p, cb, m.rne, r) == 0;
+}
+
 template <int ARCH, int ID, int K, bool RNE>
 __global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant__ DevModel m, size_t n,
                                                            const uint8_t *__restrict__ a,
@@ -261,45 +321,64 @@ __global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   // software pipeline: the next vector set's words are loaded while this one is evaluated
   uint32_t na[NW], nb[NW], nc = 0;
-  auto load = [&](size_t u) {
+  if constexpr (ARCH == MCEMU_ARCH_EXACT && !Fmt<ID>::FNUZ) {
+    // The FP32-pipe evaluation first.  A set it leaves (an Inf/NaN operand or addend,
+    // about one in six of the randomized workload, or an undecided rounding) joins a
+    // per-warp queue, and each time 32 have gathered the warp evaluates them through
+    // the table with every lane busy, instead of a divergent branch in nearly every warp.
+    __shared__ size_t queue[kF8Threads / 32][64];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t below = (1u << lane) - 1u;
+    size_t *q = queue[warp];
+    int qn = 0;                                        // warp-uniform queue length
+    size_t base = (size_t)blockIdx.x * blockDim.x + (size_t)warp * 32;
+    if (base + lane < n) f8_load<K>(a, b, c, base + lane, na, nb, nc);
+    for (; base < n; base += stride) {
+      const size_t v = base + lane;
+      uint32_t wa[NW], wb[NW];
 #pragma unroll
-    for (int w = 0; w < NW; w += 2) {
-      const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(a + u * K) + w / 2);
-      const uint2 y = __ldcs(reinterpret_cast<const uint2 *>(b + u * K) + w / 2);
-      na[w] = x.x; na[w + 1] = x.y;
-      nb[w] = y.x; nb[w + 1] = y.y;
+      for (int w = 0; w < NW; w++) { wa[w] = na[w]; wb[w] = nb[w]; }
+      const uint32_t cb = nc;
+      if (v + stride < n) f8_load<K>(a, b, c, v + stride, na, nb, nc);
+      bool defer = false;
+      if (v < n) {
+        uint32_t r;
+        if (f8_exact_fp32<ID, K>(m, wa, wb, cb, r)) __stcs(d + v, r);
+        else defer = true;
+      }
+      const uint32_t mask = __ballot_sync(0xFFFFFFFFu, defer);
+      if (mask) {
+        if (defer) q[qn + __popc(mask & below)] = v;
+        qn += __popc(mask);
+        if (qn >= 32) {
+          __syncwarp();
+          const size_t u = q[qn - 32 + lane];
+          uint32_t ua[NW], ub[NW], uc;
+          f8_load<K>(a, b, c, u, ua, ub, uc);
+          __stcs(d + u, f8_eval<ARCH, ID, K, RNE>(m, pc, tab, ua, ub, uc));
+          qn -= 32;
+          __syncwarp();
+        }
+      }
     }
-    nc = __ldcs(c + u);
-  };
+    __syncwarp();
+    if (lane < qn) {
+      const size_t u = q[lane];
+      uint32_t ua[NW], ub[NW], uc;
+      f8_load<K>(a, b, c, u, ua, ub, uc);
+      __stcs(d + u, f8_eval<ARCH, ID, K, RNE>(m, pc, tab, ua, ub, uc));
+    }
+    return;
+  }
   size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (v < n) load(v);
+  if (v < n) f8_load<K>(a, b, c, v, na, nb, nc);
   for (; v < n; v += stride) {
     uint32_t wa[NW], wb[NW];
 #pragma unroll
     for (int w = 0; w < NW; w++) { wa[w] = na[w]; wb[w] = nb[w]; }
     const uint32_t cb = nc;
-    if (v + stride < n) load(v + stride);
-    uint32_t e[K], sg[K];
-    f8_lookup<K>(tab, wa, wb, e, sg);
-    uint32_t mx = 0, orv = 0;
-#pragma unroll
-    for (int l = 0; l < K; l++) {
-      mx = max(mx, e[l]);
-      orv |= e[l];
-    }
-    uint32_t fnuz_nan = 0;
-    if constexpr (Fmt<ID>::FNUZ) {
-#pragma unroll
-      for (int w = 0; w < NW; w++) fnuz_nan |= fspecial_word<ID>(wa[w]) | fspecial_word<ID>(wb[w]);
-    }
-    uint32_t r;
-    if ((orv & 0x300u) || (cb & 0x7F800000u) == 0x7F800000u || fnuz_nan)
-      r = f8_special<ID, K>(m, e, sg, orv, cb, fnuz_nan);
-    else if constexpr (ARCH == MCEMU_ARCH_GA_EARLY)
-      r = f8_ga_early<ID, K, RNE>(m, pc, e, sg, cb, mx);
-    else
-      r = f8_exact<ID, K>(m, e, sg, cb, mx);
-    __stcs(d + v, r);
+    if (v + stride < n) f8_load<K>(a, b, c, v + stride, na, nb, nc);
+    __stcs(d + v, f8_eval<ARCH, ID, K, RNE>(m, pc, tab, wa, wb, cb));
   }
 }
 

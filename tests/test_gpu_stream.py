@@ -1,5 +1,7 @@
 """Block-FMA stream on the GPU, bit for bit against the oracle (and the paper's
 printed outputs), through the C ABI."""
+from fractions import Fraction
+
 import numpy as np
 import pytest
 
@@ -198,6 +200,56 @@ def test_exact_cancellation_and_sticky(L, fmt):
         got = gpu_block(L, spec, a, b, c)
         want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
         assert np.array_equal(got, want), f"{fmt} {name}\n" + mismatches(got, want, a, b, c)
+
+
+def _midpoint_sets(fmt, k, n, seed):
+    """Vector sets whose exact sum sits on, just above or just below a rounding
+    boundary of c: one product is +-1/2 or +-1 unit in the last place of c (a
+    product of two powers of two), some others are tiny products of either sign
+    (sticky bits), the rest zero."""
+    rng = np.random.default_rng(seed)
+    _, e, m, bias = W.fmt_params(fmt)
+    emin = 1 - bias - m                                  # smallest subnormal exponent
+    emax = (1 << e) - 2 - bias if fmt != "e4m3" else 8
+    p2 = {x: W.encode_exact(Fraction(2) ** x, fmt) for x in range(emin, emax + 1)}
+    lo_c = max(2 * emin + 24, -120) + 2
+    hi_c = min(2 * emax + 23, 120) - 2
+    ec = rng.integers(lo_c, hi_c + 1, n)
+    c = ((rng.integers(0, 2, n) << 31) | ((ec + 127) << 23) | rng.integers(0, 1 << 23, n)).astype(np.uint32)
+    dt = W.ELEM_DTYPE[fmt]
+    a = np.zeros((n, k), dtype=dt)
+    b = np.zeros((n, k), dtype=dt)
+    sgn = 1 << (8 * np.dtype(dt).itemsize - 1)
+    for v in range(n):
+        x = int(ec[v]) - 24 + int(rng.integers(0, 2))   # half an ulp of c, or a whole one
+        xa = max(emin, min(emax, x // 2))
+        xb = x - xa
+        if not (emin <= xb <= emax):
+            continue
+        a[v, 0], b[v, 0] = p2[xa], p2[xb] | (sgn if rng.random() < 0.5 else 0)
+        for l in range(1, k):
+            r = rng.random()
+            if r < 0.5:
+                continue                                 # zero product
+            ta = int(rng.integers(emin, emin + 4))
+            tb = int(rng.integers(emin, emin + 4))
+            a[v, l] = p2[ta] | (sgn if rng.random() < 0.5 else 0)
+            b[v, l] = p2[tb]
+    perm = np.argsort(rng.random((n, k)), axis=1)        # the first product anywhere in the set
+    return np.take_along_axis(a, perm, 1), np.take_along_axis(b, perm, 1), c
+
+
+@pytest.mark.parametrize("fmt,k", [("fp16", 4), ("e4m3", 8), ("e5m2", 8)])
+@pytest.mark.parametrize("out_round", ["rne", "rtz"])
+def test_exact_rounding_boundaries(L, fmt, k, out_round):
+    """Exact-then-round with RNE and RTZ on sums at, just above and just below a
+    rounding boundary (ties, sticky bits of either sign), and on independent bits."""
+    spec = dict(block_models(fmt, k)["ieee_exact"], out_round=out_round)
+    sets = [_midpoint_sets(fmt, k, 20000, seed=31), W.gen_block_fma_set(fmt, 40000, k, seed=32)]
+    for a, b, c in sets:
+        got = gpu_block(L, spec, a, b, c)
+        want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+        assert np.array_equal(got, want), f"{fmt} {out_round}\n" + mismatches(got, want, a, b, c)
 
 
 GENERIC_CASES = [
