@@ -174,12 +174,18 @@ def run_reference(args, rank):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+STREAM_SOURCES = ("core.cuh", "model.h", "stream.cu", "stream_fp8.cu")
+
+
 def kernel_source_hash():
+    """Hash of the sources the block-FMA stream kernels are compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_exact_emulation_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in STREAM_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
+    with open(os.path.join(ROOT, "include", "mcemu.h"), "rb") as f:
+        h.update(f.read())
     return h.hexdigest()[:16]
 
 

@@ -321,30 +321,44 @@ __global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   // software pipeline: the next vector set's words are loaded while this one is evaluated
   uint32_t na[NW], nb[NW], nc = 0;
-  if constexpr (ARCH == MCEMU_ARCH_EXACT && !Fmt<ID>::FNUZ) {
-    // The FP32-pipe evaluation first.  A set it leaves (an Inf/NaN operand or addend,
-    // about one in six of the randomized workload, or an undecided rounding) joins a
-    // per-warp queue, and each time 32 have gathered the warp evaluates them through
-    // the table with every lane busy, instead of a divergent branch in nearly every warp.
+  if constexpr (!(ARCH == MCEMU_ARCH_EXACT && !Fmt<ID>::FNUZ)) {
+    // the table path with special values resolved in line (cheap next to the queue
+    // below for these models)
+    size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (v < n) f8_load<K>(a, b, c, v, na, nb, nc);
+    for (; v < n; v += stride) {
+      uint32_t wa[NW], wb[NW];
+#pragma unroll
+      for (int w = 0; w < NW; w++) { wa[w] = na[w]; wb[w] = nb[w]; }
+      const uint32_t cb = nc;
+      if (v + stride < n) f8_load<K>(a, b, c, v + stride, na, nb, nc);
+      __stcs(d + v, f8_eval<ARCH, ID, K, RNE>(m, pc, tab, wa, wb, cb));
+    }
+  } else {
+    // OCP exact-then-round: the FP32-pipe evaluation first.  A set it leaves (an
+    // Inf/NaN operand or addend, about one in six of the randomized workload, or an
+    // undecided rounding) joins a per-warp queue, and each time 32 have gathered the
+    // warp evaluates them through the table with every lane busy, instead of a
+    // divergent branch in nearly every warp.
     __shared__ size_t queue[kF8Threads / 32][64];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t below = (1u << lane) - 1u;
     size_t *q = queue[warp];
-    int qn = 0;                                        // warp-uniform queue length
+    int qn = 0;                                          // warp-uniform queue length
     size_t base = (size_t)blockIdx.x * blockDim.x + (size_t)warp * 32;
     if (base + lane < n) f8_load<K>(a, b, c, base + lane, na, nb, nc);
     for (; base < n; base += stride) {
       const size_t v = base + lane;
       uint32_t wa[NW], wb[NW];
-#pragma unroll
+  #pragma unroll
       for (int w = 0; w < NW; w++) { wa[w] = na[w]; wb[w] = nb[w]; }
       const uint32_t cb = nc;
       if (v + stride < n) f8_load<K>(a, b, c, v + stride, na, nb, nc);
       bool defer = false;
       if (v < n) {
         uint32_t r;
-        if (f8_exact_fp32<ID, K>(m, wa, wb, cb, r)) __stcs(d + v, r);
-        else defer = true;
+        defer = !f8_exact_fp32<ID, K>(m, wa, wb, cb, r);
+        if (!defer) __stcs(d + v, r);
       }
       const uint32_t mask = __ballot_sync(0xFFFFFFFFu, defer);
       if (mask) {
@@ -368,17 +382,6 @@ __global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant
       f8_load<K>(a, b, c, u, ua, ub, uc);
       __stcs(d + u, f8_eval<ARCH, ID, K, RNE>(m, pc, tab, ua, ub, uc));
     }
-    return;
-  }
-  size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (v < n) f8_load<K>(a, b, c, v, na, nb, nc);
-  for (; v < n; v += stride) {
-    uint32_t wa[NW], wb[NW];
-#pragma unroll
-    for (int w = 0; w < NW; w++) { wa[w] = na[w]; wb[w] = nb[w]; }
-    const uint32_t cb = nc;
-    if (v + stride < n) f8_load<K>(a, b, c, v + stride, na, nb, nc);
-    __stcs(d + v, f8_eval<ARCH, ID, K, RNE>(m, pc, tab, wa, wb, cb));
   }
 }
 
