@@ -1127,8 +1127,11 @@ __device__ __forceinline__ uint32_t block_fma_fast(const DevModel &m, const uint
 // the hardware's RNE of that sum is t); RZ(S) is t when sign(t) r >= b and the
 // neighbour of t toward zero when sign(t) r < -b, given b < ulp(t)/4.  Everything
 // else (a result below 2^-124, an undecided rounding) is left to the integer path.
-// Returns 0 with out set, 1 when the IEEE sum is not finite (an Inf or NaN operand),
-// 2 when the rounding is not decided here.
+// The IEEE sum s of the cascade is not finite exactly when an operand or c is Inf or
+// NaN (the products cannot overflow), and its class is then the model's special
+// result: NaN for a NaN operand, Inf * 0 or Inf - Inf, else the signed Inf; that
+// result (nan_bits for NaN) is returned with the other decided ones.
+// Returns 0 with out set, 2 when the rounding is not decided here.
 __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
   s = __fadd_rn(a, b);
   const float bb = __fadd_rn(s, -a);
@@ -1136,10 +1139,15 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
 }
 
 template <int K>
-__device__ __forceinline__ int exact_fp32_sum(const float (&p)[K], uint32_t cbits, int rne, uint32_t &out) {
+__device__ __forceinline__ int exact_fp32_sum(const float (&p)[K], uint32_t cbits, int rne, uint32_t nan_bits,
+                                              uint32_t &out) {
   float s = __uint_as_float(cbits), e[K];
 #pragma unroll
   for (int l = 0; l < K; l++) two_sum(s, p[l], s, e[l]);
+  if (!(fabsf(s) <= 3.4028235e38f)) {
+    out = s != s ? nan_bits : (__float_as_uint(s) & 0x80000000u) | 0x7F800000u;
+    return 0;
+  }
   float E = e[0], a = fabsf(e[0]);
 #pragma unroll
   for (int l = 1; l < K; l++) {
@@ -1153,8 +1161,7 @@ __device__ __forceinline__ int exact_fp32_sum(const float (&p)[K], uint32_t cbit
   float t, r;
   two_sum(s, E, t, r);
   const uint32_t tb = __float_as_uint(t), ef = tb & 0x7F800000u;
-  if (ef == 0x7F800000u) return 1;
-  if (ef < (3u << 23)) return 2;                       // |t| < 2^-124: zero, subnormal, near them
+  if (ef < (3u << 23) || ef == 0x7F800000u) return 2;  // |t| < 2^-124 (zero, subnormal) or beyond
   const float pt = __uint_as_float(ef);                // 2^e_t
   if (rne) {
     if (b == 0.0f || ((tb & 0x7FFFFFu) != 0u && __fadd_ru(fabsf(r), b) < __fmul_rn(pt, 0x1p-24f))) {

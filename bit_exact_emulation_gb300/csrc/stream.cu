@@ -189,10 +189,8 @@ __global__ void __launch_bounds__(kStreamThreads) fast_kernel(const __grid_const
         p[2 * i + 1] = __fmul_rn(fa.y, fb.y);
       }
       uint32_t r = 0u;
-      const int st = exact_fp32_sum<KM>(p, cb, out_rne<RM>(m), r);
-      special = st == 1;
-      slow = st == 2;
-      if (st == 0) __stcs(d + v, r);
+      slow = exact_fp32_sum<KM>(p, cb, out_rne<RM>(m), m.nan_bits, r) != 0;
+      if (!slow) __stcs(d + v, r);
     } else if (v < n) {
       uint32_t sw = (cb & 0x7F800000u) == 0x7F800000u;
 #pragma unroll

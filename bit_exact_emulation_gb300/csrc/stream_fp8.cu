@@ -283,8 +283,8 @@ __device__ __forceinline__ void f8_load(const uint8_t *__restrict__ a, const uin
 }
 
 // Exact-then-round of one OCP FP8 set on the FP32 pipe (exact_fp32_sum): FP8 -> f16
-// -> f32 is exact, and so are the products.  False when the set has an Inf/NaN
-// operand or addend or the rounding is not decided there.
+// -> f32 is exact, and so are the products.  False when the rounding is not decided
+// there.
 template <int ID, int K>
 __device__ __forceinline__ bool f8_exact_fp32(const DevModel &m, const uint32_t (&wa)[K / 4],
                                               const uint32_t (&wb)[K / 4], uint32_t cb, uint32_t &r) {
@@ -301,7 +301,7 @@ __device__ __forceinline__ bool f8_exact_fp32(const DevModel &m, const uint32_t 
       p[4 * w + 2 * h] = __fmul_rn(fa.x, fb.x);
       p[4 * w + 2 * h + 1] = __fmul_rn(fa.y, fb.y);
     }
-  return exact_fp32_sum<K>(p, cb, m.rne, r) == 0;
+  return exact_fp32_sum<K>(p, cb, m.rne, m.nan_bits, r) == 0;
 }
 
 template <int ARCH, int ID, int K, bool RNE>
@@ -335,11 +335,9 @@ __global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant
       __stcs(d + v, f8_eval<ARCH, ID, K, RNE>(m, pc, tab, wa, wb, cb));
     }
   } else {
-    // OCP exact-then-round: the FP32-pipe evaluation first.  A set it leaves (an
-    // Inf/NaN operand or addend, about one in six of the randomized workload, or an
-    // undecided rounding) joins a per-warp queue, and each time 32 have gathered the
-    // warp evaluates them through the table with every lane busy, instead of a
-    // divergent branch in nearly every warp.
+    // OCP exact-then-round: the FP32-pipe evaluation, special values included.  A
+    // set whose rounding it leaves undecided joins a per-warp queue, and each time 32
+    // have gathered the warp evaluates them through the table with every lane busy.
     __shared__ size_t queue[kF8Threads / 32][64];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t below = (1u << lane) - 1u;
