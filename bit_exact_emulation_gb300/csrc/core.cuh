@@ -1138,6 +1138,8 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
   e = __fadd_rn(__fadd_rn(a, -__fadd_rn(s, -bb)), __fadd_rn(b, -bb));
 }
 
+__device__ __forceinline__ int exact_fp32_round(float s, float E, float b, int rne, uint32_t &out);
+
 template <int K>
 __device__ __forceinline__ int exact_fp32_sum(const float (&p)[K], uint32_t cbits, int rne, uint32_t nan_bits,
                                               uint32_t &out) {
@@ -1157,7 +1159,11 @@ __device__ __forceinline__ int exact_fp32_sum(const float (&p)[K], uint32_t cbit
   // gamma_(K-1) = (K-1) u / (1 - (K-1) u) < (K-1) 2^-23.9 <= 2^(ceil(log2(K-1)) - 23)
   constexpr float kGamma = K <= 2 ? 0x1p-23f : K <= 3 ? 0x1p-22f : K <= 5 ? 0x1p-21f : K <= 9 ? 0x1p-20f
                                                      : K <= 17 ? 0x1p-19f : 0x1p-18f;
-  const float b = __fmul_ru(a, kGamma);
+  return exact_fp32_round(s, E, __fmul_ru(a, kGamma), rne, out);
+}
+
+// The rounding step of exact_fp32_sum: S = s + E + d exactly with |d| <= b.
+__device__ __forceinline__ int exact_fp32_round(float s, float E, float b, int rne, uint32_t &out) {
   float t, r;
   two_sum(s, E, t, r);
   const uint32_t tb = __float_as_uint(t), ef = tb & 0x7F800000u;

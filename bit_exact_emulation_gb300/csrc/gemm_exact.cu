@@ -2,155 +2,143 @@
 // of AMD Matrix Cores", Secs. 4.1.1-4.1.3): every block FMA of the chain is the
 // correctly rounded value of c + sum a_l * b_l.
 //
-// Same CTA layout as the global-alignment kernel (decoded 64 x KC panels in shared
-// memory, 4 x 4 outputs per thread).  Per block and output, T bounds the top bit of
-// every term; the terms are floored into a 64-bit window of units 2^L, L = T - 61 +
-// ceil(log2(terms)), by one arithmetic shift each.  When no term lost bits the window
-// holds the exact sum and one rounding finishes the block.  Otherwise the true sum
-// lies in [W, W + terms) units; when |W| >= 2^26 the rounding boundaries of that
-// range are multiples of 4 units and the rounding of 4W and 4(W + terms) - 1 (units
-// of 2^(L-2)) brackets it: equal results are the correctly rounded sum.  Anything else
-// (a special value, heavy cancellation, a subnormal result) marks the output, and the
-// fixup pass evaluates its whole chain with the general evaluator.
+// Same CTA layout as the global-alignment kernels (64 x KC panels in shared memory,
+// 4 x 4 outputs per thread), but the panels hold each element's exact fp32 value and
+// the block FMA runs on the FP32 pipe: with every element within 2^(+-60), products of
+// at most 22 significant bits are exact normal fp32 values, and Knuth's TwoSum carries
+// the accumulator c through the block error-free.  The errors are summed by TwoSum as
+// well, so S = s + E + sum f exactly, and the leftovers f give the bound: it is 0 when
+// the error sum is exact, which decides the exact ties that few-bit products (BF16)
+// often produce.  exact_fp32_round then decides the rounding as in the stream kernels.  An element outside
+// that range, an Inf/NaN, a rounding the bound leaves undecided or a result below
+// 2^-124 or above the fp32 range marks the output, and the fixup pass evaluates its
+// whole chain with the general evaluator.
 #include "gemm_fast.cuh"
 
 namespace mcemu {
 
+// An element's exact fp32 value, or true (and 0) for an Inf/NaN or a nonzero value
+// outside [2^-60, 2^61).
+__device__ __forceinline__ bool stage_float(const FmtDev &f, uint32_t x, float &v) {
+  uint32_t S, neg;
+  int32_t E;
+  decode(f, x, S, E, neg);                           // value = S * 2^(E - m_eff), S < 2^24
+  const bool bad = classify(f, x) != 0u || (S != 0u && (E < -60 || E > 60));
+  const float w = __fmul_rn(__uint2float_rn(S), __uint_as_float((uint32_t)(E - f.m_eff + 127) << 23));
+  v = (bad || S == 0u) ? 0.0f : (neg ? -w : w);
+  return bad;
+}
+
+// Stage one K-chunk of the CTA's A rows and B columns as fp32 values, element (r, q)
+// at [q][r]; a row or column with an element stage_float rejects (or, for SPARSE,
+// invalid metadata) is flagged.
 template <int ESZ, int SPARSE>
+__device__ __forceinline__ void stage_chunk_f(const DevModel &m, int i0, int j0, int k0, int kc, int KC, int M,
+                                              int N, const uint8_t *__restrict__ A, int64_t lda,
+                                              const uint8_t *__restrict__ meta, int64_t ldm,
+                                              const uint8_t *__restrict__ Bt, int64_t ldb, float *aF, float *bF,
+                                              uint8_t *aSpec, uint8_t *bSpec) {
+  for (int e = threadIdx.x; e < kFB * KC; e += blockDim.x) {
+    const int r = e / KC, q = e % KC;
+    float v = 0.0f;
+    if constexpr (SPARSE) {
+      if (i0 + r < M && q < kc) {
+        const int kd = k0 + q, g = kd >> 2, p = kd & 3;
+        const uint32_t mb = meta[(int64_t)(i0 + r) * ldm + g];
+        const uint32_t idx0 = mb & 3u, idx1 = (mb >> 2) & 3u;
+        if (idx0 >= idx1) aSpec[r] = 1;                  // not a valid 2:4 pattern
+        const int t = (p == (int)idx0) ? 0 : (p == (int)idx1) ? 1 : -1;
+        if (t >= 0 && stage_float(m.fa, fld<ESZ>(A, (int64_t)(i0 + r) * lda + 2 * g + t), v)) aSpec[r] = 1;
+      }
+    } else {
+      if (i0 + r < M && q < kc && stage_float(m.fa, fld<ESZ>(A, (int64_t)(i0 + r) * lda + k0 + q), v))
+        aSpec[r] = 1;
+    }
+    aF[q * kFS + r] = v;
+    v = 0.0f;
+    if (j0 + r < N && q < kc && stage_float(m.fb, fld<ESZ>(Bt, (int64_t)(j0 + r) * ldb + k0 + q), v))
+      bSpec[r] = 1;
+    bF[q * kFS + r] = v;
+  }
+}
+
+template <int ESZ, int SPARSE, int RM>
 __global__ void __launch_bounds__(kFThreads, 2) gemm_exact_kernel(const __grid_constant__ DevModel m, int kt,
-                                                                int kblk, int logk, int M, int N, int K,
+                                                                int kblk, int M, int N, int K,
                                                                 const uint8_t *__restrict__ A, int64_t lda,
                                                                 const uint8_t *__restrict__ meta, int64_t ldm,
                                                                 const uint8_t *__restrict__ Bt, int64_t ldb,
                                                                 const uint32_t *C, int64_t ldc, uint32_t *D,
                                                                 int64_t ldd) {
-  extern __shared__ int32_t fsm[];
+  extern __shared__ float xsm[];
   const int KC = fast_chunk(kt);
-  int32_t *aS = fsm, *aE = aS + KC * kFS, *aG = aE + KC * kFS;
-  int32_t *bS = aG + KC * kFS, *bE = bS + KC * kFS, *bG = bE + KC * kFS;
-  uint8_t *aSpec = reinterpret_cast<uint8_t *>(bG + KC * kFS);
+  float *aF = xsm, *bF = aF + KC * kFS;                // [KC][kFS]
+  uint8_t *aSpec = reinterpret_cast<uint8_t *>(bF + KC * kFS);
   uint8_t *bSpec = aSpec + kFB;
   const int i0 = blockIdx.y * kFB, j0 = blockIdx.x * kFB;
   const int tid = threadIdx.x;
   const int ti = (tid / (kFB / kFT)) * kFT, tj = (tid % (kFB / kFT)) * kFT;
-  // B significands pre-shifted so that S_a * S_b' = U * 2^(28 - mab) < 2^30 and a
-  // product placed in the high word of a 64-bit value is U * 2^(60 - mab)
-  const int qs = 28 - m.mab;
 
-  uint32_t acc[kFT][kFT];
+  float acc[kFT][kFT];
+  uint32_t redo = 0;
 #pragma unroll
   for (int a = 0; a < kFT; a++)
 #pragma unroll
     for (int b = 0; b < kFT; b++) {
       const int i = i0 + ti + a, j = j0 + tj + b;
-      acc[a][b] = (C && i < M && j < N) ? C[(int64_t)i * ldc + j] : 0u;
+      uint32_t cb = (C && i < M && j < N) ? C[(int64_t)i * ldc + j] : 0u;
+      if ((cb & 0x7F800000u) == 0x7F800000u) redo |= 1u << (a * kFT + b);
+      if (m.c_sub_keep == 0u && (cb & 0x7F800000u) == 0u) cb &= 0x80000000u;   // flushed subnormal c
+      acc[a][b] = __uint_as_float(cb);
     }
 
-  uint32_t redo = 0;
   for (int k0 = 0; k0 < K; k0 += KC) {
     const int kc = min(KC, K - k0);
     __syncthreads();
     if (tid < kFB) { aSpec[tid] = 0; bSpec[tid] = 0; }
     __syncthreads();
-    stage_chunk<ESZ, SPARSE>(m, qs, i0, j0, k0, kc, KC, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, bS, bE, bG,
-                             aSpec, bSpec);
+    stage_chunk_f<ESZ, SPARSE>(m, i0, j0, k0, kc, KC, M, N, A, lda, meta, ldm, Bt, ldb, aF, bF, aSpec, bSpec);
     __syncthreads();
-    uint32_t rowsp = 0, colsp = 0;
 #pragma unroll
-    for (int a = 0; a < kFT; a++) rowsp |= (uint32_t)aSpec[ti + a] << a;
+    for (int a = 0; a < kFT; a++)
+      if (aSpec[ti + a]) redo |= 0xFu << (a * kFT);
 #pragma unroll
-    for (int b = 0; b < kFT; b++) colsp |= (uint32_t)bSpec[tj + b] << b;
+    for (int b = 0; b < kFT; b++)
+      if (bSpec[tj + b]) redo |= 0x1111u << b;
 
     for (int s0 = 0; s0 < kc; s0 += kt) {
       const int send = min(s0 + kt, kc);
       for (int b0 = s0; b0 < send; b0 += kblk) {
         const int nt = min(kblk, send - b0);
-        // ---- pass 1: the largest product exponent E_a + E_b
-        int32_t T[kFT][kFT];
+        // ---- the block's products, each added to c by TwoSum; the errors summed by
+        // TwoSum, with the leftovers' magnitudes rounded upward into the bound
+        float es[kFT][kFT], ea[kFT][kFT];
 #pragma unroll
         for (int a = 0; a < kFT; a++)
 #pragma unroll
-          for (int b = 0; b < kFT; b++) T[a][b] = kNegE;
+          for (int b = 0; b < kFT; b++) es[a][b] = ea[a][b] = 0.0f;
         for (int q = b0; q < b0 + nt; q++) {
-          const int4 ea = *reinterpret_cast<const int4 *>(aE + q * kFS + ti);
-          const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
-          const int32_t xa[4] = {ea.x, ea.y, ea.z, ea.w}, xb[4] = {eb.x, eb.y, eb.z, eb.w};
-#pragma unroll
-          for (int a = 0; a < kFT; a++)
-#pragma unroll
-            for (int b = 0; b < kFT; b++) T[a][b] = __viaddmax_s32(xa[a], xb[b], T[a][b]);
-        }
-        // ---- the window of each output, with c placed in it
-        int64_t W[kFT][kFT];
-        int32_t C1[kFT][kFT];
-        uint32_t st[kFT][kFT];                               // nonzero once a term lost bits
-        uint32_t nzm = 0;                                    // outputs with a nonzero product or c
-        uint32_t ovm = 0;                                    // outputs whose products may reach 2^128
-#pragma unroll
-        for (int a = 0; a < kFT; a++)
-#pragma unroll
-          for (int b = 0; b < kFT; b++) {
-            uint32_t cS, cneg;
-            int32_t cE;
-            decode_c(m, acc[a][b], cS, cE, cneg);
-            if (T[a][b] > -1024 || cS) nzm |= 1u << (a * kFT + b);
-            if (m.prod_ovf && T[a][b] >= 126) ovm |= 1u << (a * kFT + b);   // CDNA 3 product overflow
-            int32_t top = T[a][b] + 2;                       // products: |p| < 2^(E_a + E_b + 2)
-            if (cS) top = max(top, cE + 1);
-            const int32_t L = top - 61 + logk;
-            T[a][b] = L;
-            C1[a][b] = 60 + L;
-            W[a][b] = 0;
-            st[a][b] = 0;
-            if (cS) {
-              const int32_t sv = cneg ? -(int32_t)cS : (int32_t)cS;
-              const uint32_t hv = (uint32_t)sv << 6;
-              const int32_t r = 61 - cE + L;
-              W[a][b] = ((int64_t)((uint64_t)hv << 32)) >> min(r, 63);   // c * 2^38, floored
-              st[a][b] = shl_clamp(hv, (uint32_t)max(64 - r, 0));
-            }
-          }
-        // ---- pass 2: the products, floored into the window
-        for (int q = b0; q < b0 + nt; q++) {
-          const int4 sa = *reinterpret_cast<const int4 *>(aS + q * kFS + ti);
-          const int4 ea = *reinterpret_cast<const int4 *>(aE + q * kFS + ti);
-          const int4 ga = *reinterpret_cast<const int4 *>(aG + q * kFS + ti);
-          const int4 sb = *reinterpret_cast<const int4 *>(bS + q * kFS + tj);
-          const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
-          const int4 gb = *reinterpret_cast<const int4 *>(bG + q * kFS + tj);
-          const int32_t SA[4] = {sa.x, sa.y, sa.z, sa.w}, EA[4] = {ea.x, ea.y, ea.z, ea.w}, GA[4] = {ga.x, ga.y, ga.z, ga.w};
-          const int32_t SB[4] = {sb.x, sb.y, sb.z, sb.w}, EB[4] = {eb.x, eb.y, eb.z, eb.w}, GB[4] = {gb.x, gb.y, gb.z, gb.w};
+          const float4 fa = *reinterpret_cast<const float4 *>(aF + q * kFS + ti);
+          const float4 fb = *reinterpret_cast<const float4 *>(bF + q * kFS + tj);
+          const float xa[4] = {fa.x, fa.y, fa.z, fa.w}, xb[4] = {fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
           for (int a = 0; a < kFT; a++)
 #pragma unroll
             for (int b = 0; b < kFT; b++) {
-              const int32_t r = C1[a][b] - EA[a] - EB[b];
-              const int32_t v = SA[a] * SB[b] * (GA[a] * GB[b]);
-              W[a][b] += ((int64_t)((uint64_t)(uint32_t)v << 32)) >> min(r, 63);
-              // the bits dropped are the low r - 32 of v (all of v once r >= 64)
-              st[a][b] |= shl_clamp((uint32_t)v, (uint32_t)max(64 - r, 0));
+              float e, f;
+              two_sum(acc[a][b], __fmul_rn(xa[a], xb[b]), acc[a][b], e);
+              two_sum(es[a][b], e, es[a][b], f);
+              ea[a][b] = __fadd_ru(ea[a][b], fabsf(f));
             }
         }
-        // ---- rounding of the bracket
+        // ---- the correctly rounded block result
 #pragma unroll
         for (int a = 0; a < kFT; a++)
 #pragma unroll
           for (int b = 0; b < kFT; b++) {
-            const int64_t w = W[a][b];
-            const int32_t L = T[a][b];
-            uint32_t lo = 0, hi = 1;
-            bool ok = !((((rowsp >> a) | (colsp >> b)) & 1u) || (acc[a][b] & 0x7F800000u) == 0x7F800000u ||
-                        ((ovm >> (a * kFT + b)) & 1u)) &&
-                      L > kNegE / 2;
-            if (st[a][b] == 0u && w == 0)                    // exact zero: +0 unless every term is zero
-              ok = ok && ((nzm >> (a * kFT + b)) & 1u);
-            else if (st[a][b] == 0u)                         // the window holds the exact sum
-              ok = ok && hw_round64_1(w, L, m.rne, lo);
-            else
-              ok = ok && (w >= (1ll << 26) || w <= -(1ll << 26)) && hw_round64_1(4 * w, L - 2, m.rne, lo) &&
-                   hw_round64_1(4 * (w + nt + 1) - 1, L - 2, m.rne, hi) && lo == hi;
-            if (!ok) redo |= 1u << (a * kFT + b);
-            acc[a][b] = lo;
+            uint32_t r = 0u;
+            if (exact_fp32_round(acc[a][b], es[a][b], ea[a][b], RM, r)) redo |= 1u << (a * kFT + b);
+            acc[a][b] = __uint_as_float(r);
           }
       }
     }
@@ -161,7 +149,8 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_exact_kernel(const __grid_c
 #pragma unroll
     for (int b = 0; b < kFT; b++) {
       const int i = i0 + ti + a, j = j0 + tj + b;
-      if (i < M && j < N) D[(int64_t)i * ldd + j] = ((redo >> (a * kFT + b)) & 1u) ? redo_mark(m) : acc[a][b];
+      if (i < M && j < N)
+        D[(int64_t)i * ldd + j] = ((redo >> (a * kFT + b)) & 1u) ? redo_mark(m) : __float_as_uint(acc[a][b]);
     }
 }
 
@@ -176,15 +165,13 @@ template <int ESZ, int SPARSE>
 static int run_exact(const DevModel &m, int kt, int kblk, int M, int N, int K, const void *A, int64_t lda,
                      const uint8_t *meta, int64_t ldm, const void *Bt, int64_t ldb, const uint32_t *C, int64_t ldc,
                      uint32_t *D, int64_t ldd, cudaStream_t s) {
-  const size_t shm = (size_t)6 * fast_chunk(kt) * kFS * 4 + 2 * kFB;
-  auto kern = gemm_exact_kernel<ESZ, SPARSE>;
+  const size_t shm = (size_t)2 * fast_chunk(kt) * kFS * 4 + 2 * kFB;
+  auto kern = m.rne ? gemm_exact_kernel<ESZ, SPARSE, 1> : gemm_exact_kernel<ESZ, SPARSE, 0>;
   if (shm > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm) != cudaSuccess)
     return MCEMU_ERR_UNSUPPORTED;
-  int logk = 0;
-  while ((1 << logk) < kblk + 1) logk++;                 // ceil(log2(products + c))
   dim3 grid((N + kFB - 1) / kFB, (M + kFB - 1) / kFB);
-  kern<<<grid, kFThreads, shm, s>>>(m, kt, kblk, logk, M, N, K, (const uint8_t *)A, lda, meta, ldm,
+  kern<<<grid, kFThreads, shm, s>>>(m, kt, kblk, M, N, K, (const uint8_t *)A, lda, meta, ldm,
                                     (const uint8_t *)Bt, ldb, C, ldc, D, ldd);
   if (cudaGetLastError() != cudaSuccess) return MCEMU_ERR_CUDA;
   return run_fixup<ESZ, SPARSE>(m, kt, M, N, K, A, lda, meta, ldm, Bt, ldb, C, ldc, D, ldd, s);
