@@ -154,6 +154,59 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_exact_kernel(const __grid_c
     }
 }
 
+// Whole chains of the outputs gemm_exact_kernel marked, one output per thread.  Each
+// block FMA is first evaluated as in that kernel (exact fp32 values, TwoSum with an
+// error-free error sum); only a block that path does not decide (an element outside
+// 2^(+-60), an Inf/NaN, a flushed subnormal c, an undecided rounding) takes the general
+// evaluator.  A marked output thus costs about one fast chain instead of a general
+// one.  SPARSE chains run over the compressed terms (kt, K dense sizes).
+template <int ESZ, int SPARSE>
+__global__ void __launch_bounds__(256) gemm_exact_fixup_kernel(const __grid_constant__ DevModel m, int kt, int M,
+                                                               int N, int K, const uint8_t *__restrict__ A,
+                                                               int64_t lda, const uint8_t *__restrict__ meta,
+                                                               int64_t ldm, const uint8_t *__restrict__ Bt,
+                                                               int64_t ldb, const uint32_t *C, int64_t ldc,
+                                                               uint32_t *D, int64_t ldd) {
+  const int64_t tix = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (tix >= (int64_t)M * N) return;
+  const int i = (int)(tix / N), j = (int)(tix % N);
+  if (D[(int64_t)i * ldd + j] != redo_mark(m)) return;
+  const int Kc = SPARSE ? K / 2 : K, ktc = SPARSE ? kt / 2 : kt;
+  uint32_t ea[32], eb[32];
+  uint32_t acc = C ? C[(int64_t)i * ldc + j] : 0u;
+  for (int s0 = 0; s0 < Kc; s0 += ktc) {
+    const int send = min(s0 + ktc, Kc);
+    for (int b0 = s0; b0 < send; b0 += m.k) {
+      const int nt = min(m.k, send - b0);
+      bool ok = (acc & 0x7F800000u) != 0x7F800000u &&
+                !(m.c_sub_keep == 0u && (acc & 0x7F800000u) == 0u && (acc & 0x7FFFFFu) != 0u);
+      float sv = __uint_as_float(acc), es = 0.0f, bnd = 0.0f;
+      for (int l = 0; l < nt; l++) {
+        const int kc = b0 + l;
+        if constexpr (SPARSE) {
+          const uint32_t mb = meta[(int64_t)i * ldm + kc / 2];
+          const uint32_t idx = (kc & 1) ? ((mb >> 2) & 3u) : (mb & 3u);
+          ea[l] = fld<ESZ>(A, (int64_t)i * lda + kc);
+          eb[l] = fld<ESZ>(Bt, (int64_t)j * ldb + 4 * (kc / 2) + idx);
+          if ((mb & 3u) >= ((mb >> 2) & 3u)) ok = false;   // not a valid 2:4 pattern
+        } else {
+          ea[l] = fld<ESZ>(A, (int64_t)i * lda + kc);
+          eb[l] = fld<ESZ>(Bt, (int64_t)j * ldb + kc);
+        }
+        float va, vb, e, f;
+        if (stage_float(m.fa, ea[l], va) || stage_float(m.fb, eb[l], vb)) ok = false;
+        two_sum(sv, __fmul_rn(va, vb), sv, e);
+        two_sum(es, e, es, f);
+        bnd = __fadd_ru(bnd, fabsf(f));
+      }
+      uint32_t r = 0u;
+      if (!ok || exact_fp32_round(sv, es, bnd, m.rne, r)) r = block_eval_generic(m, ea, eb, nt, acc);
+      acc = r;
+    }
+  }
+  D[(int64_t)i * ldd + j] = acc;
+}
+
 // true when the exact kernel implements the model (float operands of at most 11
 // significand bits, so that products have at most 22)
 bool gemm_exact_ok(const DevModel &m) {
@@ -174,7 +227,10 @@ static int run_exact(const DevModel &m, int kt, int kblk, int M, int N, int K, c
   kern<<<grid, kFThreads, shm, s>>>(m, kt, kblk, M, N, K, (const uint8_t *)A, lda, meta, ldm,
                                     (const uint8_t *)Bt, ldb, C, ldc, D, ldd);
   if (cudaGetLastError() != cudaSuccess) return MCEMU_ERR_CUDA;
-  return run_fixup<ESZ, SPARSE>(m, kt, M, N, K, A, lda, meta, ldm, Bt, ldb, C, ldc, D, ldd, s);
+  const int64_t total = (int64_t)M * N;
+  gemm_exact_fixup_kernel<ESZ, SPARSE><<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+      m, kt, M, N, K, (const uint8_t *)A, lda, meta, ldm, (const uint8_t *)Bt, ldb, C, ldc, D, ldd);
+  return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
 }
 
 int launch_tile_gemm_exact(const DevModel &m, int kt, int M, int N, int K, const void *A, int64_t lda,
