@@ -197,7 +197,8 @@ def test_dense_bf16_2048_sampled(L):
     rng = np.random.default_rng(11)
     ii = rng.integers(0, M, 192).astype(np.int32)
     jj = rng.integers(0, N, 192).astype(np.int32)
-    for spec in (PRESETS["cdna3_bf16"], block_models("bf16", 4)["ga_trunc"], block_models("bf16", 4)["ieee_exact"]):
+    for spec in (PRESETS["cdna3_bf16"], block_models("bf16", 4)["ga_trunc"], block_models("bf16", 4)["ga_rne"],
+                 block_models("bf16", 4)["ieee_exact"]):
         m = L.Model(spec)
         D = host_u32(L.tile_gemm(m, L.tile(0, 32, 32, 8, 4), dev(A), dev(Bt), dev(C)))
         want = oracle.gemm_entries(spec, K, 8, A, Bt, C, ii, jj)
