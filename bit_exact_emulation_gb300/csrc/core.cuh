@@ -1183,6 +1183,78 @@ __device__ __forceinline__ int exact_fp32_round(float s, float E, float b, int r
   return 2;
 }
 
+// EXACT for BF16 products (which fp32 cannot hold: they span 2^+-266) on the FP32
+// pipe, with every term scaled by 2^-e_ref, e_ref = max(E_a + E_b, e_c):
+//  - a' = a * 2^(1 - E_a) lies in [2, 4) (normal a) or [2^-6, 2) (subnormal a, E_a =
+//    -126), b' likewise, so p' = a' b' is exact and p * 2^-e_ref = p' * 2^d with
+//    d = E_a + E_b - 2 - e_ref <= -2;
+//  - p' * 2^d is exact while d >= -110 (it stays normal); a product further down is
+//    dropped, and 2^-106 > |p' 2^d| joins the bound;
+//  - c * 2^-e_ref (|.| < 2) is c with its exponent field lowered by e_ref while that
+//    stays normal, else dropped with 2^-125 in the bound;
+// then the sum, its bound and the rounding decision are exact_fp32_sum's (5 terms).
+// The scaled result t' goes back by adding e_ref to its exponent field.  When that
+// reaches 2^128 the correctly rounded sum overflows: +-Inf under RNE, +-max-finite
+// under RTZ.  A subnormal result, a subnormal c and an undecided rounding return 2
+// (the integer path).  Inf/NaN operands are the caller's.  e_ref may exceed the largest
+// nonzero product's exponent (a zero operand counts with E = -126): that only moves
+// terms toward the dropped range, and the bound covers them.
+template <int K>
+__device__ __forceinline__ int exact_bf16_scaled(const uint32_t (&wa)[K / 2], const uint32_t (&wb)[K / 2],
+                                                 uint32_t cb, int rne, uint32_t &out) {
+  const uint32_t cf = (cb >> 23) & 0xFFu;
+  if (cf == 0u && (cb & 0x7FFFFFu) != 0u) return 2;        // subnormal c
+  float pp[K];
+  int32_t el[K];
+  int32_t eref = cf ? (int32_t)cf - 127 : -1000;           // c = 0 takes no part
+#pragma unroll
+  for (int i = 0; i < K / 2; i++)
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+      const uint32_t xa = h ? (wa[i] & 0xFFFF0000u) : (wa[i] << 16);   // the fp32 bits of a and b
+      const uint32_t xb = h ? (wb[i] & 0xFFFF0000u) : (wb[i] << 16);
+      const uint32_t fa = max((xa >> 23) & 0xFFu, 1u), fb = max((xb >> 23) & 0xFFu, 1u);
+      const float a1 = __fmul_rn(__uint_as_float(xa), __uint_as_float((255u - fa) << 23));
+      const float b1 = __fmul_rn(__uint_as_float(xb), __uint_as_float((255u - fb) << 23));
+      pp[2 * i + h] = __fmul_rn(a1, b1);
+      el[2 * i + h] = (int32_t)(fa + fb) - 254;
+      eref = max(eref, el[2 * i + h]);
+    }
+  float bx = 0.0f;                                          // bound of the dropped terms
+  float sv = 0.0f;
+  if (cf) {
+    if ((int32_t)cf - eref >= 1) sv = __uint_as_float(cb - ((uint32_t)eref << 23));
+    else bx = 0x1p-125f;
+  }
+  float e[K];
+#pragma unroll
+  for (int l = 0; l < K; l++) {
+    const int32_t d = el[l] - 2 - eref;
+    const bool keep = d >= -110;
+    const float sc = __uint_as_float(keep ? (uint32_t)(d + 127) << 23 : 0u);
+    if (!keep) bx = __fadd_ru(bx, 0x1p-106f);
+    two_sum(sv, __fmul_rn(pp[l], sc), sv, e[l]);
+  }
+  float E = e[0], a = fabsf(e[0]);
+#pragma unroll
+  for (int l = 1; l < K; l++) {
+    E = __fadd_rn(E, e[l]);
+    a = __fadd_ru(a, fabsf(e[l]));
+  }
+  constexpr float kGamma = K <= 2 ? 0x1p-23f : K <= 3 ? 0x1p-22f : K <= 5 ? 0x1p-21f : K <= 9 ? 0x1p-20f
+                                                     : K <= 17 ? 0x1p-19f : 0x1p-18f;
+  uint32_t tb;
+  if (exact_fp32_round(sv, E, __fadd_ru(__fmul_ru(a, kGamma), bx), rne, tb)) return 2;
+  const int32_t fr = (int32_t)((tb >> 23) & 0xFFu) + eref;
+  if (fr > 254) {                                           // the rounded sum reaches 2^128
+    out = (tb & 0x80000000u) | (rne ? 0x7F800000u : 0x7F7FFFFFu);
+    return 0;
+  }
+  if (fr < 1) return 2;                                     // a subnormal result
+  out = tb + ((uint32_t)eref << 23);
+  return 0;
+}
+
 // Powers of two (and 2^22 - 1) for fterms_w16, passed in at run time so that the
 // compiler keeps them as multiplies (FMA pipe) instead of shifts and masks (ALU).
 struct W16Consts {

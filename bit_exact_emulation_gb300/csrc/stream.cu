@@ -149,6 +149,8 @@ __global__ void __launch_bounds__(kStreamThreads) fast_kernel(const __grid_const
   constexpr bool kWords = Fmt<ID>::BYTES == 2 && Fmt<ID>::XF == 0;   // packed 16-bit decode
   // exact-then-round of FP16 sets on the FP32 pipe first (exact_fp32_sum)
   constexpr bool kFp32Exact = ARCH == MCEMU_ARCH_EXACT && ID == F_FP16;
+  // BF16 exact-then-round on the FP32 pipe with every term rescaled (exact_bf16_scaled)
+  constexpr bool kBf16Scaled = ARCH == MCEMU_ARCH_EXACT && ID == F_BF16;
   constexpr bool kDefer = ARCH == MCEMU_ARCH_EXACT && (ID == F_FP16 || ID == F_BF16 || ID == F_XF32T ||
                                                        ID == F_XF32R);
   __shared__ size_t queue[kStreamThreads / 32][64];
@@ -196,7 +198,13 @@ __global__ void __launch_bounds__(kStreamThreads) fast_kernel(const __grid_const
 #pragma unroll
       for (int i = 0; i < NW; i++) sw |= fspecial_word<ID>(wa[i]) | fspecial_word<ID>(wb[i]);
       special = sw != 0u;
-      if (!special) {
+      if constexpr (kBf16Scaled) {
+        if (!special) {
+          uint32_t r = 0u;
+          slow = exact_bf16_scaled<KM>(wa, wb, cb, out_rne<RM>(m), r) != 0;
+          if (!slow) __stcs(d + v, r);
+        }
+      } else if (!special) {
         using UT = typename std::conditional<(WIDE || ID == F_FP32), uint64_t, uint32_t>::type;
         using AT = typename std::conditional<(WIDE || ID == F_FP32), int64_t, int32_t>::type;
         uint32_t r;
