@@ -1183,43 +1183,51 @@ __device__ __forceinline__ int exact_fp32_round(float s, float E, float b, int r
   return 2;
 }
 
-// EXACT for BF16 products (which fp32 cannot hold: they span 2^+-266) on the FP32
-// pipe, with every term scaled by 2^-e_ref, e_ref = max(E_a + E_b, e_c):
-//  - a' = a * 2^(1 - E_a) lies in [2, 4) (normal a) or [2^-6, 2) (subnormal a, E_a =
-//    -126), b' likewise, so p' = a' b' is exact and p * 2^-e_ref = p' * 2^d with
-//    d = E_a + E_b - 2 - e_ref <= -2;
-//  - p' * 2^d is exact while d >= -110 (it stays normal); a product further down is
-//    dropped, and 2^-106 > |p' 2^d| joins the bound;
+// EXACT for BF16 and XF32 products (which fp32 cannot hold: they span 2^+-266 and
+// 2^+-254) on the FP32 pipe, with every term scaled by 2^-e_ref, e_ref = max(E_a + E_b,
+// e_c):
+//  - a' = a * 2^(1 - E_a) lies in [2, 4) (normal a) or, for a subnormal a (E_a = -126),
+//    in [2^-6, 2) (BF16) or [2^-9, 2) (XF32, 10 stored mantissa bits); b' likewise, so
+//    p' = a' b' is exact and p * 2^-e_ref = p' * 2^d with d = E_a + E_b - 2 - e_ref <= -2;
+//  - p' * 2^d is exact while it stays normal: d >= -110 (BF16) or -104 (XF32); a
+//    product further down is dropped, and 2^(DMIN + 4) > |p' 2^d| joins the bound;
 //  - c * 2^-e_ref (|.| < 2) is c with its exponent field lowered by e_ref while that
 //    stays normal, else dropped with 2^-125 in the bound;
-// then the sum, its bound and the rounding decision are exact_fp32_sum's (5 terms).
+// then the sum, its bound and the rounding decision are exact_fp32_sum's (K + 1 terms).
 // The scaled result t' goes back by adding e_ref to its exponent field.  When that
 // reaches 2^128 the correctly rounded sum overflows: +-Inf under RNE, +-max-finite
 // under RTZ.  A subnormal result, a subnormal c and an undecided rounding return 2
 // (the integer path).  Inf/NaN operands are the caller's.  e_ref may exceed the largest
 // nonzero product's exponent (a zero operand counts with E = -126): that only moves
 // terms toward the dropped range, and the bound covers them.
-template <int K>
-__device__ __forceinline__ int exact_bf16_scaled(const uint32_t (&wa)[K / 2], const uint32_t (&wb)[K / 2],
-                                                 uint32_t cb, int rne, uint32_t &out) {
+template <int ID, int K, int NW>
+__device__ __forceinline__ int exact_scaled(const uint32_t (&wa)[NW], const uint32_t (&wb)[NW], uint32_t cb,
+                                            int rne, uint32_t &out) {
+  static_assert(ID == F_BF16 || ID == F_XF32T, "BF16 or truncated XF32 elements");
+  constexpr int32_t DMIN = ID == F_BF16 ? -110 : -104;
+  constexpr float kDrop = ID == F_BF16 ? 0x1p-106f : 0x1p-100f;
   const uint32_t cf = (cb >> 23) & 0xFFu;
   if (cf == 0u && (cb & 0x7FFFFFu) != 0u) return 2;        // subnormal c
   float pp[K];
   int32_t el[K];
   int32_t eref = cf ? (int32_t)cf - 127 : -1000;           // c = 0 takes no part
 #pragma unroll
-  for (int i = 0; i < K / 2; i++)
-#pragma unroll
-    for (int h = 0; h < 2; h++) {
-      const uint32_t xa = h ? (wa[i] & 0xFFFF0000u) : (wa[i] << 16);   // the fp32 bits of a and b
-      const uint32_t xb = h ? (wb[i] & 0xFFFF0000u) : (wb[i] << 16);
-      const uint32_t fa = max((xa >> 23) & 0xFFu, 1u), fb = max((xb >> 23) & 0xFFu, 1u);
-      const float a1 = __fmul_rn(__uint_as_float(xa), __uint_as_float((255u - fa) << 23));
-      const float b1 = __fmul_rn(__uint_as_float(xb), __uint_as_float((255u - fb) << 23));
-      pp[2 * i + h] = __fmul_rn(a1, b1);
-      el[2 * i + h] = (int32_t)(fa + fb) - 254;
-      eref = max(eref, el[2 * i + h]);
+  for (int l = 0; l < K; l++) {
+    uint32_t xa, xb;                                        // the fp32 bits of a and b
+    if constexpr (ID == F_BF16) {
+      xa = (l & 1) ? (wa[l / 2] & 0xFFFF0000u) : (wa[l / 2] << 16);
+      xb = (l & 1) ? (wb[l / 2] & 0xFFFF0000u) : (wb[l / 2] << 16);
+    } else {
+      xa = wa[l] & 0xFFFFE000u;                             // 10 mantissa bits, truncated
+      xb = wb[l] & 0xFFFFE000u;
     }
+    const uint32_t fa = max((xa >> 23) & 0xFFu, 1u), fb = max((xb >> 23) & 0xFFu, 1u);
+    const float a1 = __fmul_rn(__uint_as_float(xa), __uint_as_float((255u - fa) << 23));
+    const float b1 = __fmul_rn(__uint_as_float(xb), __uint_as_float((255u - fb) << 23));
+    pp[l] = __fmul_rn(a1, b1);
+    el[l] = (int32_t)(fa + fb) - 254;
+    eref = max(eref, el[l]);
+  }
   float bx = 0.0f;                                          // bound of the dropped terms
   float sv = 0.0f;
   if (cf) {
@@ -1230,9 +1238,9 @@ __device__ __forceinline__ int exact_bf16_scaled(const uint32_t (&wa)[K / 2], co
 #pragma unroll
   for (int l = 0; l < K; l++) {
     const int32_t d = el[l] - 2 - eref;
-    const bool keep = d >= -110;
+    const bool keep = d >= DMIN;
     const float sc = __uint_as_float(keep ? (uint32_t)(d + 127) << 23 : 0u);
-    if (!keep) bx = __fadd_ru(bx, 0x1p-106f);
+    if (!keep) bx = __fadd_ru(bx, kDrop);
     two_sum(sv, __fmul_rn(pp[l], sc), sv, e[l]);
   }
   float E = e[0], a = fabsf(e[0]);

@@ -149,8 +149,9 @@ __global__ void __launch_bounds__(kStreamThreads) fast_kernel(const __grid_const
   constexpr bool kWords = Fmt<ID>::BYTES == 2 && Fmt<ID>::XF == 0;   // packed 16-bit decode
   // exact-then-round of FP16 sets on the FP32 pipe first (exact_fp32_sum)
   constexpr bool kFp32Exact = ARCH == MCEMU_ARCH_EXACT && ID == F_FP16;
-  // BF16 exact-then-round on the FP32 pipe with every term rescaled (exact_bf16_scaled)
-  constexpr bool kBf16Scaled = ARCH == MCEMU_ARCH_EXACT && ID == F_BF16;
+  // BF16 and truncated XF32 exact-then-round on the FP32 pipe with every term rescaled
+  // (exact_scaled)
+  constexpr bool kScaled = ARCH == MCEMU_ARCH_EXACT && (ID == F_BF16 || ID == F_XF32T);
   constexpr bool kDefer = ARCH == MCEMU_ARCH_EXACT && (ID == F_FP16 || ID == F_BF16 || ID == F_XF32T ||
                                                        ID == F_XF32R);
   __shared__ size_t queue[kStreamThreads / 32][64];
@@ -198,10 +199,10 @@ __global__ void __launch_bounds__(kStreamThreads) fast_kernel(const __grid_const
 #pragma unroll
       for (int i = 0; i < NW; i++) sw |= fspecial_word<ID>(wa[i]) | fspecial_word<ID>(wb[i]);
       special = sw != 0u;
-      if constexpr (kBf16Scaled) {
+      if constexpr (kScaled) {
         if (!special) {
           uint32_t r = 0u;
-          slow = exact_bf16_scaled<KM>(wa, wb, cb, out_rne<RM>(m), r) != 0;
+          slow = exact_scaled<ID, KM, NW>(wa, wb, cb, out_rne<RM>(m), r) != 0;
           if (!slow) __stcs(d + v, r);
         }
       } else if (!special) {

@@ -239,7 +239,7 @@ def _midpoint_sets(fmt, k, n, seed):
     return np.take_along_axis(a, perm, 1), np.take_along_axis(b, perm, 1), c
 
 
-@pytest.mark.parametrize("fmt,k", [("fp16", 4), ("bf16", 4), ("e4m3", 8), ("e5m2", 8)])
+@pytest.mark.parametrize("fmt,k", [("fp16", 4), ("bf16", 4), ("xf32", 2), ("e4m3", 8), ("e5m2", 8)])
 @pytest.mark.parametrize("out_round", ["rne", "rtz"])
 def test_exact_rounding_boundaries(L, fmt, k, out_round):
     """Exact-then-round with RNE and RTZ on sums at, just above and just below a
