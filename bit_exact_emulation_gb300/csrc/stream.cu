@@ -2,8 +2,10 @@
 // per thread, eq. (1) of "Accurate Models of AMD Matrix Cores" under the model.
 //
 // The data are read once, so the kernel is a grid-stride stream of 8-, 16- or
-// 32-byte vector loads with the evict-first cache hint; the work per vector is
-// integer ALU (decode, significand products, max, shifts, one normalisation).
+// 32-byte vector loads with the evict-first cache hint.  The work per vector is
+// integer ALU (decode, significand products, max, shifts, one normalisation) for the
+// alignment models; exact-then-round runs on the FP32 pipe (exact products, TwoSum)
+// and leaves the sets it does not decide to the integer path, batched per warp.
 #include <cuda_runtime.h>
 
 #include "core.cuh"
