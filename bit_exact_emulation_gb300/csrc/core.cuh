@@ -1197,7 +1197,8 @@ __device__ __forceinline__ int exact_fp32_round(float s, float E, float b, int r
 // The scaled result t' goes back by adding e_ref to its exponent field.  When that
 // reaches 2^128 the correctly rounded sum overflows: +-Inf under RNE, +-max-finite
 // under RTZ.  A subnormal result, a subnormal c and an undecided rounding return 2
-// (the integer path).  Inf/NaN operands are the caller's.  e_ref may exceed the largest
+// (the integer path).  Inf/NaN operands and the CDNA 3 product-overflow rule are the
+// caller's.  e_ref may exceed the largest
 // nonzero product's exponent (a zero operand counts with E = -126): that only moves
 // terms toward the dropped range, and the bound covers them.
 template <int ID, int K, int NW>

@@ -201,13 +201,18 @@ __global__ void __launch_bounds__(kStreamThreads) fast_kernel(const __grid_const
 #pragma unroll
       for (int i = 0; i < NW; i++) sw |= fspecial_word<ID>(wa[i]) | fspecial_word<ID>(wb[i]);
       special = sw != 0u;
+      bool done = special;
       if constexpr (kScaled) {
-        if (!special) {
+        // the rescaled products are exact, so a model that turns products of 2^128 or
+        // more into Inf (the CDNA 3 rule) keeps the integer path
+        if (!done && !m.prod_ovf) {
           uint32_t r = 0u;
           slow = exact_scaled<ID, KM, NW>(wa, wb, cb, out_rne<RM>(m), r) != 0;
           if (!slow) __stcs(d + v, r);
+          done = true;
         }
-      } else if (!special) {
+      }
+      if (!done) {
         using UT = typename std::conditional<(WIDE || ID == F_FP32), uint64_t, uint32_t>::type;
         using AT = typename std::conditional<(WIDE || ID == F_FP32), int64_t, int32_t>::type;
         uint32_t r;
