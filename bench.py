@@ -317,6 +317,9 @@ def main():
                     help="comma list of the GEMM workloads to time (dense, sparse, multiword)")
     ap.add_argument("--vectors", type=int, default=N_VEC,
                     help="vector sets per (format, model) launch; smaller values are for profiling runs only")
+    ap.add_argument("--only", default="",
+                    help="profiling runs only: comma list of format:model stream launches to keep (e.g. "
+                         "bf16:ieee_exact); the end-to-end, GEMM and CPU legs are skipped")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -343,13 +346,18 @@ def main():
         return torch.from_numpy(x).cuda()
 
     n_vec = args.vectors
+    only = {tuple(x.split(":")) for x in args.only.split(",") if x}
     # inputs: this rank's own vector sets (weak scaling)
     data, gpu, launches = {}, {}, []
     for fmt, k in FORMATS:
+        if only and not any(f == fmt for f, _ in only):
+            continue
         a, b, c = W.gen_block_fma_set(fmt, n_vec, k, seed=rank_seed(k, rank))
         data[fmt] = (a, b, c)
         gpu[fmt] = (dev(a), dev(b), dev(c))
         for name, desc in workload_models(fmt, k):
+            if only and (fmt, name) not in only:
+                continue
             m = L.Model(desc)
             d = torch.empty(n_vec, dtype=torch.int32, device="cuda")
             launches.append((fmt, name, m, d))
@@ -413,6 +421,12 @@ def main():
                 "algorithmic_bytes_per_launch": algo_bytes,
                 "per_kernel_gbs": {f"{f} {n}": n_vec * (2 * VEC_BYTES[f] + 8) / (t / 1e3) / 1e9
                                    for (f, n, _, _), t in zip(launches, per_launch)}}
+
+    if only:
+        if rank == 0:
+            print(json.dumps({"profiling_only": sorted(f"{f}:{n}" for f, n in only), "vectors": n_vec,
+                              "ms_per_step": ms_per_step, "roofline": roofline}), flush=True)
+        return
 
     # end to end through the host-buffer entry point (pinned host memory, copies timed)
     e2e = None

@@ -179,9 +179,16 @@ __device__ __forceinline__ uint32_t round_pack32(uint32_t M, int32_t lsb, uint32
 // Hardware rounding of an integer significand: value = S * 2^k.  The int->fp32
 // conversion rounds S to 24 bits exactly as the model's RNE or RTZ does, and
 // scaling by powers of two is exact while the result stays normal; an overflow
-// gives Inf under RN and the largest finite under RZ, as the model does.  A
-// subnormal result would be rounded twice, so those (and zero) return false
-// and the caller takes the integer path.
+// gives Inf under RN and the largest finite under RZ, as the model does.  An
+// exact value below 2^-126 would be rounded twice: first to 24 bits, which can
+// carry it up to the subnormal tie 2^-126 - 2^-150 or onto 2^-126 itself, then
+// onto the subnormal grid.  Rounding is monotonic and 2^-126 is on both grids,
+// so such a value always lands at or below 2^-126, and a result above 2^-126
+// in magnitude proves the exact value was normal.  A result of magnitude 2^-126
+// or less (zero, subnormal, or 2^-126 itself) returns false and the caller takes
+// the integer path.
+__device__ __forceinline__ bool hw_normal(uint32_t bits) { return (bits & 0x7FFFFFFFu) > 0x00800000u; }
+
 __device__ __forceinline__ bool hw_scale(float x, int32_t k, int rne, uint32_t &bits) {
   const int32_t k1 = min(max(k, -96), 96);           // |x| in [1, 2^63): x*2^k1 stays normal
   const int32_t k2 = min(k - k1, 127);                // beyond 127 the result overflows anyway
@@ -190,7 +197,7 @@ __device__ __forceinline__ bool hw_scale(float x, int32_t k, int rne, uint32_t &
   const float s2 = __uint_as_float((uint32_t)(k2 + 127) << 23);
   const float y = rne ? __fmul_rn(__fmul_rn(x, s1), s2) : __fmul_rz(__fmul_rz(x, s1), s2);
   bits = __float_as_uint(y);
-  return (bits & 0x7F800000u) != 0u;
+  return hw_normal(bits);
 }
 // The same with one multiply when 2^k is a normal float (the common case of the GEMM
 // merges; the stream kernels keep the branch-free two-multiply form).
@@ -198,7 +205,7 @@ __device__ __forceinline__ bool hw_scale1(float x, int32_t k, int rne, uint32_t 
   if ((uint32_t)(k + 126) <= 253u) {
     const float s = __uint_as_float((uint32_t)(k + 127) << 23);
     bits = __float_as_uint(rne ? __fmul_rn(x, s) : __fmul_rz(x, s));
-    return (bits & 0x7F800000u) != 0u;
+    return hw_normal(bits);
   }
   return hw_scale(x, k, rne, bits);
 }

@@ -134,14 +134,15 @@ __device__ __forceinline__ uint32_t f8_special(const DevModel &m, const uint32_t
 }
 
 // fp32 bits of S * 2^k, S != 0 an integer, rounded (RNE or RZ) in hardware; false
-// when the result is subnormal or k is out of the single-multiply range
+// when k is out of the single-multiply range or the result is 2^-126 or below in
+// magnitude (where the two roundings could differ from one, see hw_scale)
 template <bool RNE>
 __device__ __forceinline__ bool f8_round(int32_t S, int32_t k, uint32_t &bits) {
   if ((uint32_t)(k + 126) > 253u) return false;
   const float x = RNE ? __int2float_rn(S) : __int2float_rz(S);
   const float sc = __uint_as_float((uint32_t)(k + 127) << 23);
   bits = __float_as_uint(RNE ? __fmul_rn(x, sc) : __fmul_rz(x, sc));
-  return (bits & 0x7F800000u) != 0u;
+  return hw_normal(bits);
 }
 
 // Early-c global alignment (Table 3): e_max over the products, c and e_min^lim;

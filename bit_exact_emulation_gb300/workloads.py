@@ -341,3 +341,68 @@ def gen_multiword_fp64(M: int, N: int, K: int, seed: int = 5):
         return rng.standard_normal(shape) * np.exp2(rng.uniform(-20.0, 20.0, size=shape))
 
     return one((M, K)), one((N, K))
+
+
+def gen_subnormal_boundary(fmt: str, n: int, k: int, seed: int):
+    """Vector sets whose exact sum lies within a few units of 2^-150 of +-2^-126, the
+    boundary between the largest fp32 subnormal and the smallest normal: at, just
+    above and just below the subnormal ties 2^-126 - 2^-150 and 2^-126 + 2^-150 (half
+    the subnormal spacing), with sticky products of either sign far below.  Formats
+    whose products reach that far down: bf16, xf32, fp32 (k >= 2).
+
+    Each set has a lead that sits on the boundary -- a product +-2^-126, an addend
+    +-(2^-126 + r 2^-149), two products +-2^-125 -+ 2^-126 or two halves +-2^-127, or
+    a subnormal addend just below 2^-126 -- then an offset product -+q 2^(t-152)
+    (q < 64, |t| <= 2) and, for half of the sets, a product +-2^(-153-u).  Every
+    product is realised as (q 2^x) * 2^y with both factors normal, the rest of the
+    block holds zero products, and the products are shuffled within the block."""
+    if fmt not in ("bf16", "xf32", "fp32") or k < 2:
+        raise ValueError("bf16/xf32/fp32 operands and k >= 2")
+    rng = np.random.default_rng(seed)
+    dt = ELEM_DTYPE[fmt]
+    cache = {}
+
+    def code(q: int, x: int) -> int:
+        key = (q, x)
+        if key not in cache:
+            cache[key] = encode_exact(Fraction(q) * Fraction(2) ** x, fmt)
+        return cache[key]
+
+    one = code(1, 0)
+    a = np.zeros((n, k), dtype=np.uint64)
+    b = np.full((n, k), one, dtype=np.uint64)
+    c = np.zeros(n, dtype=np.uint64)
+    for v in range(n):
+        s = int(rng.integers(0, 2))                     # sign of the lead
+        terms = []                                      # (negative, q, exponent)
+        lead = int(rng.integers(0, 5 if k >= 3 else 4))
+        cbits = None
+        if lead == 0:
+            terms.append((s, 1, -126))
+        elif lead == 1:
+            cbits = (s << 31) | (0x00800000 + int(rng.integers(0, 3)))
+        elif lead == 2:
+            cbits = (s << 31) | (0x00800000 - int(rng.integers(1, 4)))
+        elif lead == 3:
+            terms.append((s, 1, -127))
+            cbits = (s << 31) | 0x00400000
+        else:
+            pair = int(rng.integers(0, 2))
+            terms += [(s, 1, -125), (1 - s, 1, -126)] if pair == 0 else [(s, 1, -127), (s, 1, -127)]
+        q = int(rng.integers(0, 64))
+        if q and len(terms) < k:
+            toward = 1 - s if rng.random() < 0.75 else s  # mostly down to the ties below
+            terms.append((toward, q, int(rng.integers(-2, 3)) - 152))
+        if rng.random() < 0.5 and len(terms) < k:
+            terms.append((int(rng.integers(0, 2)), 1, -153 - int(rng.integers(0, 41))))
+        if cbits is None:
+            r = rng.random()
+            cbits = 0 if r < 0.7 else (0x80000000 if r < 0.8 else
+                                       (int(rng.integers(0, 2)) << 31) | int(rng.integers(1, 4)))
+        pos = rng.permutation(k)[:len(terms)]
+        for (neg, qq, x), p in zip(terms, pos):
+            xa = x // 2                                 # q 2^xa times 2^(x - xa)
+            a[v, p] = code(qq, xa) | (int(neg) << (8 * np.dtype(dt).itemsize - 1))
+            b[v, p] = code(1, x - xa)
+        c[v] = cbits
+    return a.astype(dt), b.astype(dt), c.astype(np.uint32)

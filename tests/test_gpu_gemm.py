@@ -135,6 +135,33 @@ def test_early_c_gemm_exponent_ranges(L, case):
     assert len(bad) == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
 
 
+GEMM_BOUNDARY = [  # format, model, instruction K
+    ("bf16", PRESETS["cdna3_bf16"], 8), ("bf16", block_models("bf16", 4)["ga_rne"], 8),
+    ("bf16", block_models("bf16", 4)["ga_trunc"], 8), ("bf16", block_models("bf16", 4)["ieee_exact"], 8),
+    ("xf32", PRESETS["cdna3_xf32"], 8), ("xf32", block_models("xf32", 2)["ieee_exact"], 8),
+    ("bf16", PRESETS["b200_bf16"], 16),
+]
+
+
+@pytest.mark.parametrize("case", range(len(GEMM_BOUNDARY)))
+def test_gemm_subnormal_boundary(L, case):
+    """The tile GEMM on sums next to 2^-126: row i of A and of B^T is one boundary
+    vector set (with C[i][:] its addend), so every diagonal output is a set that sits
+    at or near a tie of the subnormal grid; the off-diagonal ones mix sets.  Every
+    output against the oracle (the fast kernels send these chains to the fixup pass)."""
+    fmt, spec, kt = GEMM_BOUNDARY[case]
+    k = spec["n_fma"]
+    n = 96
+    a, b, c = W.gen_subnormal_boundary(fmt, n, k, seed=90 + case)
+    A, Bt = np.ascontiguousarray(a), np.ascontiguousarray(b)
+    C = np.repeat(c.reshape(n, 1), n, axis=1)
+    m = L.Model(spec)
+    D = host_u32(L.tile_gemm(m, L.tile(0, 16, 16, kt, 4), dev(A), dev(Bt), dev(C)))
+    ii, jj = all_entries(n, n)
+    want = oracle.gemm_entries(spec, k, kt, A, Bt, C, ii, jj).reshape(n, n)
+    bad = np.argwhere(D != want)
+    assert len(bad) == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
+
 def test_tile_gemm_specials_and_zero_k(L):
     spec = PRESETS["cdna3_bf16"]
     A, Bt, C = operands("bf16", 20, 20, 64, seed=5, special_rate=0.03)

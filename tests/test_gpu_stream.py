@@ -252,6 +252,37 @@ def test_exact_rounding_boundaries(L, fmt, k, out_round):
         assert np.array_equal(got, want), f"{fmt} {out_round}\n" + mismatches(got, want, a, b, c)
 
 
+BOUNDARY_MODELS = [  # format, block size, model
+    ("bf16", 4, block_models("bf16", 4)["ga_rne"]), ("bf16", 4, block_models("bf16", 4)["ga_trunc"]),
+    ("bf16", 4, block_models("bf16", 4)["ieee_exact"]),
+    ("bf16", 4, dict(block_models("bf16", 4)["ieee_exact"], out_round="rtz")),
+    ("xf32", 2, block_models("xf32", 2)["ga_rne"]), ("xf32", 2, block_models("xf32", 2)["ga_trunc"]),
+    ("xf32", 2, block_models("xf32", 2)["ieee_exact"]),
+    ("xf32", 2, dict(block_models("xf32", 2)["ieee_exact"], out_round="rtz")),
+    ("bf16", 8, PRESETS["cdna3_bf16"]), ("xf32", 4, PRESETS["cdna3_xf32"]),
+    ("bf16", 16, PRESETS["b200_bf16"]), ("xf32", 8, PRESETS["b200_tf19"]),
+    ("bf16", 2, PRESETS["cdna1_bf16"]), ("fp32", 2, dict(PRESETS["cdna1_fp32"], n_fma=2)),
+    ("bf16", 4, dict(block_models("bf16", 4)["ga_rne"], align_frac=40)),
+    ("bf16", 5, dict(block_models("bf16", 4)["ga_rne"], n_fma=5)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(BOUNDARY_MODELS)))
+def test_subnormal_boundary(L, case):
+    """Exact sums at, just above and just below the ties next to 2^-126 (largest subnormal
+    / smallest normal), with sticky products of both signs: a result must be rounded
+    once, onto the subnormal grid, never first to 24 bits and then again."""
+    fmt, k, spec = BOUNDARY_MODELS[case]
+    a, b, c = W.gen_subnormal_boundary(fmt, 20000, k, seed=70 + case)
+    got = gpu_block(L, spec, a, b, c)
+    want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+    assert np.array_equal(got, want), f"{fmt} k={k}\n" + mismatches(got, want, a, b, c)
+    if fmt == "bf16" and k == 4:
+        # the hand-traced set 2^-126 - 1.25 * 2^-150: the largest subnormal under every model
+        a1 = np.array([[0x2000, 0x9A20, 0, 0]], np.uint16)
+        b1 = np.array([[0x2000, 0x1A00, 0x3F80, 0x3F80]], np.uint16)
+        assert int(gpu_block(L, spec, a1, b1, np.zeros(1, np.uint32))[0]) == 0x007FFFFF
+
 @pytest.mark.parametrize("fmt,k", [("bf16", 4), ("xf32", 2)])
 @pytest.mark.parametrize("prod_overflow", [False, True])
 def test_exact_wide_formats_product_overflow(L, fmt, k, prod_overflow):

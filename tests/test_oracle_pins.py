@@ -85,6 +85,38 @@ def test_exact_model_bf16_extreme_spread():
         assert d[v] == exact_spec.exact_block("bf16", a[v], b[v], c[v], nan_bits=spec["nan_bits"])
 
 
+
+@pytest.mark.parametrize("fmt,k", [("bf16", 4), ("xf32", 2), ("bf16", 8)])
+@pytest.mark.parametrize("mode", ["rne", "rtz"])
+def test_exact_model_at_the_subnormal_boundary(fmt, k, mode):
+    """Sums within a few 2^-150 of +-2^-126 (the ties of the subnormal grid next to the
+    smallest normal, sticky bits of both signs): the exact model is the correctly
+    rounded sum, rounded once onto the subnormal grid (IEEE 754 Sec. 4.3; "Accurate
+    Models of AMD Matrix Cores", Sec. 4.1 keeps subnormals)."""
+    a, b, c = W.gen_subnormal_boundary(fmt, 1500, k, seed=3 + k)
+    spec = dict(block_models(fmt, k)["ieee_exact"], out_round=mode)
+    d = oracle.block_fma(spec, a, b, c)
+    for v in range(len(c)):
+        want = exact_spec.exact_block(fmt, a[v], b[v], c[v], mode, nan_bits=spec["nan_bits"])
+        assert d[v] == want, (fmt, v, a[v], b[v], hex(c[v]), hex(d[v]), hex(want))
+
+
+def test_subnormal_tie_hand_traced():
+    """a = (2^-63, -1.25 * 2^-75, 0, 0), b = (2^-63, 2^-75, 1, 1), c = +0 in bf16: the
+    sum is 2^-126 - 1.25 * 2^-150, a quarter of a subnormal step below the tie at
+    2^-126 - 2^-150.  Every term lies on the global-alignment grid 2^-152 (e_max = -126,
+    F_p = 26), so truncation, RNE and the exact model all give the largest subnormal
+    0x007FFFFF; rounding to 24 bits first would reach the tie and round up to 2^-126."""
+    a = np.array([[0x2000, 0x9A20, 0, 0]], np.uint16)
+    b = np.array([[0x2000, 0x1A00, 0x3F80, 0x3F80]], np.uint16)
+    c = np.zeros(1, np.uint32)
+    for name in ("ga_trunc", "ga_rne", "ieee_exact"):
+        assert int(oracle.block_fma(block_models("bf16", 4)[name], a, b, c)[0]) == 0x007FFFFF, name
+    # one unit of 2^-152 less below the tie rounds the other way under RNE only
+    a2 = np.array([[0x2000, 0x9A00, 0, 0]], np.uint16)     # 2^-126 - 2^-150: the tie itself
+    assert int(oracle.block_fma(block_models("bf16", 4)["ga_rne"], a2, b, c)[0]) == 0x00800000
+    assert int(oracle.block_fma(block_models("bf16", 4)["ga_trunc"], a2, b, c)[0]) == 0x007FFFFF
+
 @pytest.mark.parametrize("fmt", ["e5m2", "e4m3"])
 def test_exact_fp8_exhaustive_pairs(fmt):
     """Every (a, b) pair of an 8-bit format, K = 1, against a set of addends."""
