@@ -21,7 +21,8 @@ PRESET = {"cdna3_fp16": 0, "cdna3_bf16": 1, "cdna3_xf32": 2, "cdna3_fp8": 3, "cd
           "cdna1_fp16": 5, "cdna1_bf16": 6, "cdna1_fp32": 7, "cdna2_fp16": 8, "cdna2_bf16_1k": 9,
           "cdna2_bf16": 10, "b200_fp16": 11, "h100_fp16": 12, "a100_fp16": 13, "b200_bf16": 14,
           "a100_bf16": 15, "b200_tf19": 16, "a100_tf19": 17, "b200_fp8": 18, "h100_fp8": 19,
-          "ga_trunc": 100, "ga_rne": 101, "ieee_exact": 102}
+          "b200_fp16_f16": 20, "h100_fp16_f16": 21, "a100_fp16_f16": 22, "b200_fp8_f16": 23,
+          "h100_fp8_f16": 24, "ga_trunc": 100, "ga_rne": 101, "ieee_exact": 102}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "not 2:4 sparse", 4: "alignment",
           5: "CUDA error", 6: "timeout", 7: "workspace too small"}
 FRO_OUT_DOUBLES = 1026
@@ -68,6 +69,7 @@ SYMBOLS = {
                         + [ctypes.c_void_p, ctypes.c_int64] * 4 + [ctypes.c_void_p]),
     "mcemu_sparse24_compress": (ctypes.c_int, [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_int64] * 3
                                 + [ctypes.c_void_p, ctypes.c_void_p]),
+    "mcemu_sparse24_check": (ctypes.c_int, [ctypes.c_void_p] * 3),
     "mcemu_sparse24_expand": (ctypes.c_int, [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_int64] * 3
                               + [ctypes.c_void_p]),
     "mcemu_sparse24_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 3
@@ -111,7 +113,7 @@ def desc_from_spec(spec: dict) -> ModelDesc:
     """Model description from the named-feature dict used across the project
     (keys: fmt_a, fmt_b, fp8_enc, xf32_round, arch, n_fma, align_frac, align_round,
     c_frac, psum_frac, post_norm_frac, out_round, sub_in_flush, sub_out_flush,
-    c_zero_exp, emin_lim, prod_overflow, nan_bits, int_saturate, pair_group)."""
+    c_zero_exp, emin_lim, prod_overflow, nan_bits, int_saturate, pair_group, acc_fmt)."""
     d = ModelDesc()
     d.struct_size = ctypes.sizeof(ModelDesc)
     d.fmt_a, d.fmt_b = FMT[spec["fmt_a"]], FMT[spec["fmt_b"]]
@@ -124,7 +126,7 @@ def desc_from_spec(spec: dict) -> ModelDesc:
     d.c_frac_bits = int(spec.get("c_frac", 24))
     d.psum_frac_bits = int(spec.get("psum_frac", 32))
     d.post_norm_frac_bits = int(spec.get("post_norm_frac", 31))
-    d.acc_sig_bits = 24
+    d.acc_sig_bits = {"fp32": 24, "fp16": 11}[spec.get("acc_fmt", "fp32")]
     d.out_round = {"rne": 0, "rtz": 1}[spec.get("out_round", "rne")]
     d.subnormal_in_flush = int(bool(spec.get("sub_in_flush", False)))
     d.subnormal_out_flush = int(bool(spec.get("sub_out_flush", False)))
@@ -214,8 +216,10 @@ def tile_gemm(model: Model, t: TileDesc, A, Bt, C, D=None):
     return D
 
 
-def sparse24_compress(fmt: str, A, fp8_enc: str = "ocp"):
-    """(Ac [M][K/2], meta [M][K/4] uint8, violations int64 tensor on the device)."""
+def sparse24_compress(fmt: str, A, fp8_enc: str = "ocp", check: bool = False):
+    """(Ac [M][K/2], meta [M][K/4] uint8, violations int64 tensor on the device).
+    With check=True the call waits for the stream and raises McemuError with status
+    MCEMU_ERR_NOT_2_4 (3) when a group of four held more than two nonzeros."""
     import torch
     M, K = A.shape
     Ac = torch.empty((M, K // 2), dtype=A.dtype, device=A.device)
@@ -224,6 +228,8 @@ def sparse24_compress(fmt: str, A, fp8_enc: str = "ocp"):
     _check(lib().mcemu_sparse24_compress(FMT[fmt], {"ocp": 0, "fnuz": 1}[fp8_enc], M, K, _p(A), A.stride(0),
                                          _p(Ac), Ac.stride(0), _p(meta), meta.stride(0), _p(viol),
                                          _stream()), "mcemu_sparse24_compress")
+    if check:
+        _check(lib().mcemu_sparse24_check(_p(viol), None, _stream()), "mcemu_sparse24_check")
     return Ac, meta, viol
 
 

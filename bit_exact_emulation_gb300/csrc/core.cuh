@@ -838,10 +838,76 @@ __device__ __forceinline__ uint32_t block_int(const DevModel &m, const uint32_t 
 }  // namespace mcemu
 
 namespace mcemu {
+// A block FMA whose addend and result are binary16 (the fp16 output of Table 3's
+// note, "Accurate Models of AMD Matrix Cores"): the early-c global alignment or the
+// exact model, FP16/FP8 operands.  Every product of those formats and the binary16 c
+// are multiples of 2^-48 below 2^37 in magnitude, so each term is an exact 128-bit
+// integer in units of 2^-48; global alignment cuts the terms to the grid
+// 2^(e_max - F_p) (toward zero, or down), and the sum is rounded once to 11 bits
+// (exponents -14 .. 15, subnormal grid 2^-24).  c is the low half of cbits.
+static __device__ __noinline__ uint32_t block_eval_acc16(const DevModel &m, const uint32_t *ea, const uint32_t *eb,
+                                                         int nt, uint32_t cbits) {
+  constexpr int32_t kG = -48;                    // unit of the exact terms
+  const uint32_t ch = cbits & 0xFFFFu;
+  uint32_t spec = 0;
+  for (int l = 0; l < nt; l++) spec |= product_special(m, ea[l], eb[l]);
+  if ((ch & 0x7C00u) == 0x7C00u) spec |= (ch & 0x3FFu) ? 1u : ((ch >> 15) ? 4u : 2u);
+  if (spec) return ((spec & 1u) || (spec & 6u) == 6u) ? m.nan_bits : ((spec & 2u) ? 0x7C00u : 0xFC00u);
+  const uint32_t cef = (ch >> 10) & 0x1Fu, cneg = ch >> 15;
+  const uint32_t cS = cef ? ((ch & 0x3FFu) | 0x400u) : (ch & m.c_sub_keep);
+  const int32_t cE = (int32_t)(cef ? cef : 1u) - 15;
+  Term<uint64_t> p[32];
+  int32_t emax = m.emin_lim;
+  bool all_neg_zero = cS == 0u && cneg;
+  for (int l = 0; l < nt; l++) {
+    p[l] = make_term<uint64_t>(m, ea[l], eb[l]);
+    if (p[l].U) emax = max(emax, p[l].e);
+    all_neg_zero = all_neg_zero && p[l].U == 0 && p[l].neg;
+  }
+  emax = max(emax, cS ? cE : m.c_zero_exp);
+  // the alignment grid in units of 2^-48 (no cut when it is not above the unit)
+  const int32_t cut = (m.arch == MCEMU_ARCH_GA_EARLY) ? emax - m.F - kG : 0;
+  i128 S = 0;
+  for (int l = 0; l <= nt; l++) {
+    u128 v;
+    uint32_t neg;
+    if (l < nt) {
+      if (!p[l].U) continue;
+      v = (u128)p[l].U << (p[l].e - m.mab - kG);  // U * 2^(e - mab), e - mab >= -48
+      neg = p[l].neg;
+    } else {
+      if (!cS) continue;
+      v = (u128)cS << (cE - 10 - kG);
+      neg = cneg;
+    }
+    if (cut > 0) {                               // cut <= 88: the model's exponents are checked
+      const u128 low = v & (((u128)1 << cut) - 1);
+      v -= low;                                  // toward zero on the magnitude
+      if (m.align_rd && neg && low) v += (u128)1 << cut;   // floor of a negative term
+    }
+    S += neg ? -(i128)v : (i128)v;
+  }
+  if (S == 0) return all_neg_zero ? 0x8000u : 0u;
+  const uint32_t neg = S < 0 ? 1u : 0u;
+  const u128 M = neg ? (u128)(-S) : (u128)S;
+  const uint64_t hi = (uint64_t)(M >> 64), lo = (uint64_t)M;
+  const int32_t msb = hi ? 127 - __clzll((long long)hi) : 63 - __clzll((long long)lo);
+  const int32_t Ec = max(msb + kG, -14);         // exponent of the result, floored at e_min
+  const int32_t r = Ec - 10 - kG;                // bits below the binary16 grid: >= 24
+  const uint32_t q = (uint32_t)(M >> r);         // < 2^11
+  const u128 rem = M & (((u128)1 << r) - 1), half = (u128)1 << (r - 1);
+  const bool up = m.rne && (rem > half || (rem == half && (q & 1u)));
+  uint32_t bits = ((uint32_t)(Ec + 14) << 10) + q + (up ? 1u : 0u);
+  if (Ec > 15 || bits >= 0x7C00u) bits = m.rne ? 0x7C00u : 0x7BFFu;
+  if (m.sub_out_flush && bits < 0x0400u) bits = 0u;
+  return bits | (neg << 15);
+}
+
 // Any model, any block size up to 32: one out-of-line copy per translation unit
 // for the general (non-specialised) kernels.  64-bit significand arithmetic.
 static __device__ __noinline__ uint32_t block_eval_generic(const DevModel &m, const uint32_t *ea,
                                                            const uint32_t *eb, int nt, uint32_t cbits) {
+  if (m.acc16) return block_eval_acc16(m, ea, eb, nt, cbits);
   uint32_t a[32], b[32];
   bool anys = (cbits & 0x7F800000u) == 0x7F800000u;
 #pragma unroll

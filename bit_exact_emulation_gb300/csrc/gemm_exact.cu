@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(256) gemm_exact_fixup_kernel(const __grid_cons
 // true when the exact kernel implements the model (float operands of at most 11
 // significand bits, so that products have at most 22)
 bool gemm_exact_ok(const DevModel &m) {
-  if (m.fa.is_int || m.fb.is_int || m.arch != MCEMU_ARCH_EXACT) return false;
+  if (m.fa.is_int || m.fb.is_int || m.arch != MCEMU_ARCH_EXACT || m.acc16) return false;
   return m.mab <= 22 && m.k <= 32;
 }
 

@@ -6,7 +6,7 @@ namespace mcemu {
 
 // true when the fast kernel implements the model (else the general kernel runs)
 bool gemm_fast_ok(const DevModel &m) {
-  if (m.fa.is_int || m.fb.is_int) return false;
+  if (m.fa.is_int || m.fb.is_int || m.acc16) return false;
   if (m.arch != MCEMU_ARCH_GA_EARLY && m.arch != MCEMU_ARCH_GA_LATE) return false;
   if (m.wide || m.align_rd || m.sub_out_flush) return false;
   if (m.mab > 22) return false;                          // binary32 significands: 48-bit products

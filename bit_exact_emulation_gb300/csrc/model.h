@@ -53,6 +53,7 @@ struct DevModel {
   int32_t bias_sum;       // bias_a + bias_b (products carry biased exponents)
   int32_t wide;           // 1 when sums need 64-bit integers
   uint32_t p0mul, p0cmul; // 2^P0 and 2^P0c (32-bit sums): the pre-shifts as multiplies
+  int32_t acc16;          // 1: c and d are binary16 (low half of the 32-bit words)
 };
 
 struct Model {

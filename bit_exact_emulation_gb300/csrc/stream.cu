@@ -371,7 +371,7 @@ int launch_block_fma(const DevModel &m, size_t n, const void *a, const void *b, 
   const int id = fmt_id(m);
   if (id >= 0 && f8_stream_ok(m, id)) return launch_block_fma_f8(m, id, n, a, b, c, d, stream);
   // the specialised kernels assume kept subnormals (the fp32 special-value shortcut)
-  if (id >= 0 && m.arch != MCEMU_ARCH_PAIRWISE && m.fa.sub_keep != 0u && m.c_sub_keep != 0u) {
+  if (id >= 0 && !m.acc16 && m.arch != MCEMU_ARCH_PAIRWISE && m.fa.sub_keep != 0u && m.c_sub_keep != 0u) {
     for (const Special &sp : kSpecial) {
       if (sp.arch != m.arch || sp.id != id || sp.km != m.k) continue;
       if (m.arch != MCEMU_ARCH_EXACT && sp.wide != (m.wide != 0)) continue;

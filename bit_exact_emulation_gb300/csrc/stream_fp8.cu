@@ -392,6 +392,7 @@ __global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant
 // subnormals kept
 bool f8_stream_ok(const DevModel &m, int id) {
   if (id != F_E4M3 && id != F_E4M3Z && id != F_E5M2 && id != F_E5M2Z) return false;
+  if (m.acc16) return false;
   if (m.fa.sub_keep == 0u || m.c_sub_keep == 0u || m.sub_out_flush) return false;
   if (m.k != 8 && m.k != 16 && m.k != 32) return false;
   if (m.arch == MCEMU_ARCH_EXACT) return true;

@@ -255,12 +255,19 @@ def gen_block_fma_set(fmt: str, n: int, k: int, seed: int, enc: str = "ocp",
     return a, b, c
 
 
+def algorithm3_rng(seed: int = 0):
+    """The Mersenne Twister (MT19937) stream of Algorithm 3 ("mt19937 rng(0)")."""
+    return np.random.Generator(np.random.MT19937(seed))
+
+
 def gen_exp_mantissa(fmt: str, n: int, k: int, e_ab: tuple, e_c: tuple, seed: int = 0,
-                     enc: str = "ocp"):
+                     enc: str = "ocp", rng=None):
     """Exponent-mantissa sampling (Sec. 5.1, Algorithm 3): significand ~ U(-2+2^(1-f),
     2-2^(1-f)), exponent ~ U{e-, ..., e+}; the value is rounded to the format (RNE).
-    A Mersenne Twister (MT19937) seeded with `seed` drives the draws."""
-    rng = np.random.Generator(np.random.MT19937(seed))
+    A Mersenne Twister (MT19937) seeded with `seed` drives the draws; pass `rng` (from
+    algorithm3_rng) instead to draw a large ensemble in consecutive chunks of one stream."""
+    if rng is None:
+        rng = algorithm3_rng(seed)
     dt, e, m, bias = fmt_params(fmt if fmt != "xf32" else "fp32", enc)
     f = m + 1 if fmt != "xf32" else 11
 

@@ -92,14 +92,16 @@ typedef struct {
   int32_t c_frac_bits;           /* GA_LATE/ODD_EVEN: shifted c kept to this (24)    */
   int32_t psum_frac_bits;        /* GA_LATE/ODD_EVEN: shifted product sum (32)      */
   int32_t post_norm_frac_bits;   /* GA_LATE/ODD_EVEN: after normalisation (31)       */
-  int32_t acc_sig_bits;          /* significand of the fp32 result: must be 24       */
+  int32_t acc_sig_bits;          /* significand of c and d: 24 (binary32), or 11     */
+                                 /* (binary16 in the low half of each 32-bit c and d */
+                                 /* word; GA_EARLY or EXACT with FP16/FP8 inputs)    */
   int32_t out_round;             /* MCEMU_OUT_RNE or MCEMU_OUT_RTZ                   */
   int32_t subnormal_in_flush;    /* 1: subnormal inputs (a, b, c) count as zero      */
   int32_t subnormal_out_flush;   /* 1: subnormal results become zero                 */
   int32_t c_zero_exp;            /* exponent of c = 0 (-126 on CDNA 3) or NO_EXP     */
   int32_t emin_lim;              /* GA_EARLY: floor of e_max (Table 3) or NO_EXP     */
   int32_t prod_overflow_2p128;   /* 1: a product with |p| >= 2^128 becomes +-Inf     */
-  uint32_t nan_bits;             /* fp32 pattern of every NaN result                 */
+  uint32_t nan_bits;             /* pattern of every NaN result (binary16 for 11)    */
   int32_t int_saturate;          /* INT formats: clamp the int32 sum instead of wrap */
   int32_t pair_group;            /* PAIRWISE: products per group (= block_k)         */
 } mcemu_model_desc;
@@ -130,6 +132,13 @@ enum {
   MCEMU_PRESET_A100_TF19 = 17,   /* (2,24), N_FMA 4                                  */
   MCEMU_PRESET_B200_FP8 = 18,    /* (2,25), N_FMA 32, no e_min limit                 */
   MCEMU_PRESET_H100_FP8 = 19,    /* (2,13), N_FMA 32                                 */
+  /* Table 3's note: fp16 output (acc_sig_bits 11) for fp16 and fp8 inputs, with
+   * e_min^lim -21 (H100, B200) or -20 (A100); c and d are binary16 */
+  MCEMU_PRESET_B200_FP16_F16 = 20, /* as B200_FP16, fp16 c and d, e_min^lim -21      */
+  MCEMU_PRESET_H100_FP16_F16 = 21,
+  MCEMU_PRESET_A100_FP16_F16 = 22, /* as A100_FP16, fp16 c and d, e_min^lim -20      */
+  MCEMU_PRESET_B200_FP8_F16 = 23,  /* as B200_FP8, fp16 c and d, e_min^lim -21       */
+  MCEMU_PRESET_H100_FP8_F16 = 24,
   MCEMU_PRESET_GA_TRUNC = 100,
   MCEMU_PRESET_GA_RNE = 101,
   MCEMU_PRESET_IEEE_EXACT = 102
@@ -213,6 +222,11 @@ int mcemu_tile_gemm(mcemu_model_t model, const mcemu_tile_desc *tile, int M, int
 int mcemu_sparse24_compress(int fmt, int fp8_enc, int M, int K, const void *A, int64_t lda,
                             void *Ac, int64_t ldac, uint8_t *meta, int64_t ldm,
                             int64_t *d_violations, void *stream);
+/* Synchronous check of a compression: waits for `stream`, reads the device
+ * counter *d_violations into *h_count (when not NULL) and returns
+ * MCEMU_ERR_NOT_2_4 when some group held more than two nonzeros (the pattern of
+ * "Structured sparsity (2:4 pattern)" does not hold), MCEMU_OK otherwise. */
+int mcemu_sparse24_check(const int64_t *d_violations, int64_t *h_count, void *stream);
 /* Inverse: A = expand(Ac, meta), zeros elsewhere. */
 int mcemu_sparse24_expand(int fmt, int M, int K, const void *Ac, int64_t ldac,
                           const uint8_t *meta, int64_t ldm, void *A, int64_t lda, void *stream);

@@ -36,7 +36,8 @@ class Model(ctypes.Structure):
         "c_frac", "psum_frac", "post_norm_frac", "out_round", "sub_in", "sub_out",
         "c_zero_exp", "emin_lim", "prod_ovf")] + [("nan_bits", ctypes.c_uint32),
                                                   ("int_sat", ctypes.c_int32),
-                                                  ("pair_group", ctypes.c_int32)]
+                                                  ("pair_group", ctypes.c_int32),
+                                                  ("acc_fmt", ctypes.c_int32)]
 
     @classmethod
     def from_spec(cls, spec: dict) -> "Model":
@@ -64,6 +65,7 @@ class Model(ctypes.Structure):
         m.nan_bits = int(spec.get("nan_bits", 0x7FC00000))
         m.int_sat = int(bool(spec.get("int_saturate", False)))
         m.pair_group = int(spec.get("pair_group", spec["n_fma"]))
+        m.acc_fmt = {"fp32": 0, "fp16": 1}[spec.get("acc_fmt", "fp32")]
         return m
 
 

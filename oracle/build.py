@@ -12,7 +12,8 @@ LIB_PATH = os.path.join(HERE, "liborc.so")
 
 def build_oracle(force: bool = False) -> str:
     src = os.path.join(HERE, "orc.c")
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= os.path.getmtime(src):
+    newest = max(os.path.getmtime(src), os.path.getmtime(os.path.join(HERE, "orc.h")))
+    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
         return LIB_PATH
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",

@@ -248,13 +248,14 @@ static term make_product(const orc_model *md, num a, num b) {
   return p;
 }
 
+/* The addend in the accumulator format: binary32, or binary16 from the low half. */
 static term make_c(const orc_model *md, uint32_t cbits) {
-  num c = decode(ORC_FP32, 0, 0, cbits);
-  if (md->sub_in && c.cls == CL_FIN && c.S < (1u << 23)) { c.cls = CL_ZERO; c.S = 0; }
+  num c = md->acc_fmt == ORC_ACC_FP16 ? decode(ORC_FP16, 0, 0, cbits & 0xFFFFu) : decode(ORC_FP32, 0, 0, cbits);
+  if (md->sub_in && c.cls == CL_FIN && c.S < ((uint64_t)1 << c.m)) { c.cls = CL_ZERO; c.S = 0; }
   term t;
   t.cls = c.cls; t.neg = c.neg; t.e = c.E;
   big_zero(&t.v);
-  if (c.cls == CL_FIN) big_from(&t.v, c.neg, c.S, c.E - 23);
+  if (c.cls == CL_FIN) big_from(&t.v, c.neg, c.S, c.E - c.m);
   return t;
 }
 
@@ -287,6 +288,36 @@ static uint32_t to_fp32(const big *v, int out_round, int flush_sub, int zero_neg
   return bits | (neg ? 0x80000000u : 0u);
 }
 
+/* Round v to binary16 (11-bit significand, exponents -14 .. 15, subnormal grid
+ * 2^-24) with RNE or RTZ; overflow gives Inf under RNE and +-65504 under RTZ. */
+static uint32_t to_fp16(const big *v, int out_round, int flush_sub, int zero_neg) {
+  if (big_is_zero(v)) return zero_neg ? 0x8000u : 0u;
+  int neg = v->neg;
+  int E = big_log2(v);
+  if (E < -14) E = -14;                        /* subnormal grid 2^-24 */
+  big r;
+  big_round_grid(&r, v, E - 10, out_round == ORC_RNE ? GRID_RNE : GRID_RZ);
+  if (big_is_zero(&r)) return neg ? 0x8000u : 0u;
+  int E2 = big_log2(&r);
+  if (E2 > 15)
+    return (neg ? 0x8000u : 0u) | (out_round == ORC_RNE ? 0x7C00u : 0x7BFFu);
+  uint32_t bits;
+  if (E2 < -14) {
+    if (flush_sub) return neg ? 0x8000u : 0u;
+    bits = (uint32_t)big_bits(&r, -24 + ORC_FIX, 10);
+  } else {
+    uint32_t q = (uint32_t)big_bits(&r, E2 - 10 + ORC_FIX, 11);
+    bits = ((uint32_t)(E2 + 15) << 10) | (q & 0x3FFu);
+  }
+  return bits | (neg ? 0x8000u : 0u);
+}
+
+/* The result in the accumulator format. */
+static uint32_t to_acc(const orc_model *md, const big *v, int zero_neg) {
+  if (md->acc_fmt == ORC_ACC_FP16) return to_fp16(v, md->out_round, md->sub_out, zero_neg);
+  return to_fp32(v, md->out_round, md->sub_out, zero_neg);
+}
+
 /* Sign of an exactly-zero result: negative only when every product is a
  * negative zero and c is -0 (IEEE 754 rule for sums of zeros under RNE/RTZ). */
 static int zero_sign(const term *p, int n, const term *c) {
@@ -306,8 +337,9 @@ static int special_result(const orc_model *md, const term *p, int n, const term 
     if (t->cls == CL_INF) { if (t->neg) ninf = 1; else pinf = 1; }
   }
   if (pinf && ninf) { *d = md->nan_bits; return 1; }
-  if (pinf) { *d = 0x7F800000u; return 1; }
-  if (ninf) { *d = 0xFF800000u; return 1; }
+  const int h = md->acc_fmt == ORC_ACC_FP16;
+  if (pinf) { *d = h ? 0x7C00u : 0x7F800000u; return 1; }
+  if (ninf) { *d = h ? 0xFC00u : 0xFF800000u; return 1; }
   return 0;
 }
 
@@ -320,7 +352,7 @@ static int special_result(const orc_model *md, const term *p, int n, const term 
 static uint32_t arch_exact(const orc_model *md, const term *p, int n, const term *c) {
   big V = c->v;
   for (int l = 0; l < n; l++) big_add(&V, &V, &p[l].v);
-  return to_fp32(&V, md->out_round, md->sub_out, zero_sign(p, n, c));
+  return to_acc(md, &V, zero_sign(p, n, c));
 }
 
 /* Global alignment with early c (Table 3, NVIDIA columns): c joins the
@@ -348,7 +380,7 @@ static uint32_t arch_ga_early(const orc_model *md, const term *p, int n, const t
     big_round_grid(&t, &c->v, g, mode);
     big_add(&S, &S, &t);
   }
-  return to_fp32(&S, md->out_round, md->sub_out, zero_sign(p, n, c));
+  return to_acc(md, &S, zero_sign(p, n, c));
 }
 
 /* Algorithm 1 (CDNA 3 fp16/bf16/tf32 inputs), lines 3-15, with the late-c
@@ -553,6 +585,15 @@ static int model_ok(const orc_model *md) {
   if (md->n_fma < 1 || md->n_fma > 64) return 0;
   if (!orc_elem_bytes(md->fmt_a) || !orc_elem_bytes(md->fmt_b)) return 0;
   if (is_int_fmt(md->fmt_a) != is_int_fmt(md->fmt_b)) return 0;
+  if (md->acc_fmt != ORC_ACC_FP32 && md->acc_fmt != ORC_ACC_FP16) return 0;
+  if (md->acc_fmt == ORC_ACC_FP16) {
+    /* fp16 output: fp16 and fp8 inputs, the exact and early-c architectures */
+    if (md->arch != ORC_EXACT && md->arch != ORC_GA_EARLY) return 0;
+    for (int i = 0; i < 2; i++) {
+      int f = i ? md->fmt_b : md->fmt_a;
+      if (f != ORC_FP16 && f != ORC_E4M3 && f != ORC_E5M2) return 0;
+    }
+  }
   return 1;
 }
 

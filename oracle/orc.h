@@ -57,7 +57,15 @@ typedef struct {
   uint32_t nan_bits;         /* fp32 pattern returned for every NaN result               */
   int32_t int_sat;           /* INT inputs: 1 = saturate the int32 result, 0 = wrap      */
   int32_t pair_group;        /* pairwise arch: products per group (4 or 2)               */
+  int32_t acc_fmt;           /* c and d: ORC_ACC_FP32, or ORC_ACC_FP16 (binary16 in the  */
+                             /* low half of each 32-bit c and d word; Table 3 note)      */
 } orc_model;
+
+/* Accumulator (c and d) formats.  Table 3's note in "Accurate Models of AMD Matrix
+ * Cores": NVIDIA tensor cores also write fp16 for fp8 and fp16 inputs, with
+ * e_min^lim = -20 (A100) or -21 (H100/B200).  Taken with the EXACT and GA_EARLY
+ * architectures and fp16/fp8 inputs only. */
+enum { ORC_ACC_FP32 = 0, ORC_ACC_FP16 = 1 };
 
 #ifdef __cplusplus
 extern "C" {

@@ -20,10 +20,12 @@ and the correctly rounded model.  Keys (all optional except fmt/arch/n_fma):
   prod_overflow     |p| >= 2^128 gives Inf
   nan_bits          fp32 bit pattern of every NaN result
   int_saturate      integer formats: clamp the int32 result instead of wrapping
+  acc_fmt           fp32 | fp16: format of c and d (fp16 in the low half of each 32-bit word)
 """
 
 CDNA_NAN = 0xFFC00000     # "the resulting NaN carries a negative sign" (Secs. 4.1-4.3)
 GENERIC_NAN = 0x7FC00000
+GENERIC_NAN16 = 0x7E00    # the quiet NaN of binary16 (fp16-output models)
 
 
 def _cdna3(fmt, n_fma, **kw):
@@ -82,6 +84,12 @@ PRESETS = {
     "a100_tf19": _early("xf32", 4, 24, "rtz", emin_lim=-132),
     "b200_fp8": _early("e4m3", 32, 25, "rtz"),
     "h100_fp8": _early("e4m3", 32, 13, "rtz"),
+    # Table 3's note: fp16 output for fp16 and fp8 inputs, e_min^lim -20 (A100) / -21 (H100, B200)
+    "b200_fp16_f16": _early("fp16", 16, 25, "rtz", emin_lim=-21, acc_fmt="fp16", nan_bits=GENERIC_NAN16),
+    "h100_fp16_f16": _early("fp16", 16, 25, "rtz", emin_lim=-21, acc_fmt="fp16", nan_bits=GENERIC_NAN16),
+    "a100_fp16_f16": _early("fp16", 8, 24, "rtz", emin_lim=-20, acc_fmt="fp16", nan_bits=GENERIC_NAN16),
+    "b200_fp8_f16": _early("e4m3", 32, 25, "rtz", emin_lim=-21, acc_fmt="fp16", nan_bits=GENERIC_NAN16),
+    "h100_fp8_f16": _early("e4m3", 32, 13, "rtz", emin_lim=-21, acc_fmt="fp16", nan_bits=GENERIC_NAN16),
 }
 
 

@@ -72,8 +72,35 @@ def round_fp32(x: Fraction, mode: str = "rne", zero_neg: bool = False) -> int:
     return sign | ((e + 127) << 23) | (n - (1 << 23))
 
 
-def exact_block(fmt, a_bits, b_bits, c_bits, mode="rne", enc="ocp", nan_bits=0x7FC00000):
-    """Correctly rounded sum_l a_l*b_l + c with IEEE special-value rules."""
+def round_fp16(x: Fraction, mode: str = "rne", zero_neg: bool = False) -> int:
+    """binary16 bits of x rounded once (RNE or toward zero) onto the binary16 grid:
+    11-bit significands, exponents -14 .. 15, subnormal spacing 2^-24; overflow gives
+    Inf under RNE and the largest finite value (65504) under RTZ."""
+    if x == 0:
+        return 0x8000 if zero_neg else 0
+    sign = 0x8000 if x < 0 else 0
+    ax = abs(x)
+    e = ax.numerator.bit_length() - ax.denominator.bit_length()
+    if Fraction(2) ** e > ax:
+        e -= 1
+    e = max(e, -14)
+    q = ax / Fraction(2) ** (e - 10)
+    n = q.numerator // q.denominator
+    r = q - n
+    if mode == "rne" and (r > Fraction(1, 2) or (r == Fraction(1, 2) and n % 2 == 1)):
+        n += 1
+    if n == 1 << 11:
+        n, e = 1 << 10, e + 1
+    if e > 15:
+        return sign | (0x7C00 if mode == "rne" else 0x7BFF)
+    if n < (1 << 10):
+        return sign | n
+    return sign | ((e + 15) << 10) | (n - (1 << 10))
+
+
+def exact_block(fmt, a_bits, b_bits, c_bits, mode="rne", enc="ocp", nan_bits=0x7FC00000, acc="fp32"):
+    """Correctly rounded sum_l a_l*b_l + c with IEEE special-value rules; with acc="fp16"
+    c is the binary16 in the low half of c_bits and the result is binary16."""
     prods = []
     for x, y in zip(a_bits, b_bits):
         u, v = decode(fmt, int(x), enc), decode(fmt, int(y), enc)
@@ -89,7 +116,7 @@ def exact_block(fmt, a_bits, b_bits, c_bits, mode="rne", enc="ocp", nan_bits=0x7
             prods.append(NINF if su != sv else PINF)
         else:
             prods.append((u[0] * v[0], u[1] != v[1]))
-    c = decode("fp32", int(c_bits))
+    c = decode("fp16", int(c_bits) & 0xFFFF) if acc == "fp16" else decode("fp32", int(c_bits))
     if c == NAN:
         return nan_bits
     terms = prods + [c]
@@ -97,7 +124,9 @@ def exact_block(fmt, a_bits, b_bits, c_bits, mode="rne", enc="ocp", nan_bits=0x7
     if len(infs) == 2:
         return nan_bits
     if infs:
+        if acc == "fp16":
+            return 0x7C00 if PINF in infs else 0xFC00
         return 0x7F800000 if PINF in infs else 0xFF800000
     total = sum(t[0] for t in terms)
     zero_neg = all(t[0] == 0 and t[1] for t in terms)
-    return round_fp32(total, mode, zero_neg)
+    return round_fp16(total, mode, zero_neg) if acc == "fp16" else round_fp32(total, mode, zero_neg)

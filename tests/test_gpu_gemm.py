@@ -162,6 +162,28 @@ def test_gemm_subnormal_boundary(L, case):
     bad = np.argwhere(D != want)
     assert len(bad) == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
 
+@pytest.mark.parametrize("name", ["b200_fp16_f16", "a100_fp16_f16", "h100_fp8_f16"])
+def test_gemm_fp16_output(L, name):
+    """Tile GEMM with the fp16 accumulator: C and D hold binary16 in the low half of
+    each 32-bit word, and every block's binary16 result is the next block's addend."""
+    spec = PRESETS[name]
+    fmt = spec["fmt_a"]
+    M, N, K, kt = 37, 29, 96, 2 * spec["n_fma"]
+    rng = np.random.default_rng(7)
+    A = W.independent_bits(rng, fmt, (M, K), "ocp", 0.005)
+    Bt = W.independent_bits(rng, fmt, (N, K), "ocp", 0.005)
+    if fmt == "fp16":                                   # keep most chains finite
+        A = (A & np.uint16(0xBFFF)).astype(np.uint16)
+        Bt = (Bt & np.uint16(0xBFFF)).astype(np.uint16)
+    C = W.independent_bits(rng, "fp16", (M, N), "ocp", 0.005).astype(np.uint32)
+    m = L.Model(spec)
+    D = host_u32(L.tile_gemm(m, L.tile(0, 16, 16, kt, 4), dev(A), dev(Bt), dev(C)))
+    ii, jj = all_entries(M, N)
+    want = oracle.gemm_entries(spec, K, kt, A, Bt, C, ii, jj).reshape(M, N)
+    bad = np.argwhere(D != want)
+    assert len(bad) == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
+    assert (D >> 16).max() == 0
+
 def test_tile_gemm_specials_and_zero_k(L):
     spec = PRESETS["cdna3_bf16"]
     A, Bt, C = operands("bf16", 20, 20, 64, seed=5, special_rate=0.03)
@@ -249,6 +271,26 @@ def test_sparse24_compress_matches_oracle(L, fmt, enc):
     assert np.array_equal(meta.cpu().numpy(), rmeta)
     assert int(viol.item()) == rviol and rviol > 0
 
+
+def test_sparse24_violation_raises_not_2_4(L):
+    """A group of four with three nonzeros: the device counter reports it, and the
+    synchronous check returns MCEMU_ERR_NOT_2_4 (the 2:4 pattern does not hold)."""
+    A, _, _ = W.gen_sparse_e4m3(8, 8, 64, seed=4)
+    ok_Ac, _, v0 = L.sparse24_compress("e4m3", dev(A), check=True)   # a valid pattern passes
+    assert int(v0.item()) == 0
+    bad = A.copy()
+    g = bad[3, 8:12]
+    bad[3, 8:12] = np.where(g == 0, np.uint8(0x38), g)[:4]          # fill the zeros: 4 nonzeros
+    bad[5, 20:24] = [0x38, 0x40, 0x48, 0]                            # 3 nonzeros
+    Ac, meta, viol = L.sparse24_compress("e4m3", dev(bad))
+    torch.cuda.synchronize()
+    assert int(viol.item()) == 2
+    with pytest.raises(L.McemuError) as e:
+        L.sparse24_compress("e4m3", dev(bad), check=True)
+    assert e.value.status == 3
+    want_Ac, want_meta, want_v = oracle.sparse24_compress("e4m3", bad)
+    assert want_v == 2
+    assert np.array_equal(Ac.cpu().numpy(), want_Ac) and np.array_equal(meta.cpu().numpy(), want_meta)
 
 def test_sparse24_expand_inverts_compress(L):
     A, Bt, C = W.gen_sparse_e4m3(64, 8, 256, seed=4)

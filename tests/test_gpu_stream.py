@@ -297,6 +297,40 @@ def test_exact_wide_formats_product_overflow(L, fmt, k, prod_overflow):
         assert np.array_equal(got, want), f"{fmt} {out_round} {prod_overflow}\n" + mismatches(got, want, a, b, c)
 
 
+F16_OUT = ["b200_fp16_f16", "h100_fp16_f16", "a100_fp16_f16", "b200_fp8_f16", "h100_fp8_f16"]
+
+
+@pytest.mark.parametrize("name", F16_OUT)
+@pytest.mark.parametrize("variant", ["preset", "exact_rne", "rd_flush", "e5m2"])
+def test_fp16_output_models(L, name, variant):
+    """Table 3's note: fp16 c and d (binary16 in the low half of each word) for fp16 and
+    fp8 inputs, e_min^lim -20/-21, RTZ; plus the exact model with RNE, round-down
+    alignment with flushed subnormals, and E5M2 operands.  Independent bits with
+    specials, and exponent-mantissa sets down at the limit."""
+    spec = dict(PRESETS[name])
+    if variant == "exact_rne":
+        spec.update(arch="exact", out_round="rne")
+    elif variant == "rd_flush":
+        spec.update(align_round="rd", sub_in_flush=True, sub_out_flush=True)
+    elif variant == "e5m2":
+        if spec["fmt_a"] != "e4m3":
+            pytest.skip("fp16 operands")
+        spec.update(fmt_a="e5m2", fmt_b="e5m2")
+    fmt, k = spec["fmt_a"], spec["n_fma"]
+    rng = np.random.default_rng(80)
+    a, b, _ = W.gen_block_fma_set(fmt, 20000, k, seed=81, special_rate=0.01)
+    c = W.independent_bits(rng, "fp16", (20000,), "ocp", 0.01).astype(np.uint32)
+    sets = [(a, b, c)]
+    lo = {"fp16": (-24, -12), "e4m3": (-9, -4), "e5m2": (-16, -8)}[fmt]
+    a2, b2, _ = W.gen_exp_mantissa(fmt, 20000, k, lo, (-14, 15), seed=0)
+    c2 = W.gen_exp_mantissa("fp16", 20000, 1, (-24, -10), (-14, 15), seed=1)[0].reshape(-1).astype(np.uint32)
+    sets.append((a2, b2, c2))
+    for a, b, c in sets:
+        got = gpu_block(L, spec, a, b, c)
+        want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+        assert np.array_equal(got, want), f"{name} {variant}\n" + mismatches(got, want, a, b, c)
+        assert (got >> 16).max() == 0
+
 GENERIC_CASES = [
     ("exact", "fp16", 1), ("exact", "bf16", 3), ("ga_early", "bf16", 5), ("ga_late", "fp16", 12),
     ("odd_even", "e4m3", 32), ("ga_early", "e5m2", 32), ("pairwise", "bf16", 8), ("exact", "xf32", 16),
@@ -331,6 +365,38 @@ def test_mixed_fp8_operands(L):
     want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
     assert np.array_equal(got, want), mismatches(got, want)
 
+
+FP8_ADDENDS = ["0", "-0", "2^-149", "-1", "3*2^-30", "1.5*2^20", "-2^-20", "0.75", "-448", "2^-126"]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("enc", ["ocp", "fnuz"])
+def test_fp8_all_pairs(L, fmt, enc):
+    """Every (a, b) pair of the 8-bit format against a set of addends: K = 1 (the general
+    evaluator) and K = 8 with the pair among seven zero products (the product-table
+    kernel), for truncation, RNE and exact-then-round, and the CDNA 3 Algorithm 2
+    preset (K = 16)."""
+    codes = np.arange(256, dtype=np.uint8)
+    a1 = np.repeat(codes, 256)
+    b1 = np.tile(codes, 256)
+    n = a1.size
+    cs = np.array([W.encode_exact(W.parse_value(x), "fp32") for x in FP8_ADDENDS], np.uint32)
+    models = {name: dict(spec, fp8_enc=enc) for name, spec in block_models(fmt, 8).items()}
+    models["cdna3"] = dict(PRESETS["cdna3_fp8" if fmt == "e4m3" else "cdna3_bf8"], fp8_enc=enc)
+    rng = np.random.default_rng(9)
+    for name, spec in models.items():
+        for k in (1, spec["n_fma"]):
+            s = dict(spec, n_fma=k)
+            pos = rng.integers(0, k, n)                       # where the pair sits in the block
+            a = np.zeros((n, k), np.uint8)
+            b = np.zeros((n, k), np.uint8)
+            a[np.arange(n), pos] = a1
+            b[np.arange(n), pos] = b1
+            for cb in cs:
+                c = np.full(n, cb, np.uint32)
+                got = gpu_block(L, s, a, b, c)
+                want = oracle.block_fma_parallel(s, a, b, c, threads=8)
+                assert np.array_equal(got, want), f"{fmt} {enc} {name} k={k} c={cb:#x}\n" + mismatches(got, want)
 
 @pytest.mark.parametrize("sat", [False, True])
 @pytest.mark.parametrize("fa,fb", [("int8", "int8"), ("uint8", "uint8"), ("int8", "uint8")])

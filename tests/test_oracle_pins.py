@@ -8,6 +8,7 @@
 import ctypes
 import ctypes.util
 import itertools
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -381,3 +382,121 @@ def test_table2_bounds():
     for n, printed in ((1e5, 1.38e-4), (1e6, 1.38e-5), (1e7, 1.38e-6), (2e6, 6.91e-6), (2e7, 6.91e-7)):
         p = -expm1(log(eps) / (n + 1))
         assert abs(p - printed) / printed < 0.005
+
+
+def test_table2_bounds_of_the_harness():
+    """The validation harness's p_eps: Table 2's m = 0 rows, and for m = 1 the (1 - eps)
+    quantile of the Beta(2, N) posterior of Sec. 5.4 (1.669e-5 at N = 10^6; the printed
+    1.69e-5 and 1.35e-5 for N = 1.25 * 10^6 are that quantile rounded up)."""
+    pytest.importorskip("scipy")
+    import validate_algorithm3 as V
+    for n, printed in ((10**6, 1.38e-5), (10**7, 1.38e-6), (2 * 10**7, 6.91e-7), (2 * 10**6, 6.91e-6)):
+        assert abs(V.p_eps(n, 0) - printed) / printed < 0.005
+    # m = 1: solve (N + 1) N \int_0^p t (1 - t)^(N - 1) dt = 1 - eps by bisection, independently of scipy
+    from math import exp, log1p
+    for n, want in ((10**6, 1.669e-5), (1_250_000, 1.335e-5)):
+        def cdf(p):   # regularized incomplete beta I_p(2, N) = 1 - (1 - p)^N (1 + N p)
+            return 1.0 - exp(n * log1p(-p)) * (1.0 + n * p)
+        lo, hi = 0.0, 1e-3
+        for _ in range(200):
+            mid = (lo + hi) / 2
+            lo, hi = (mid, hi) if cdf(mid) < 1 - 1e-6 else (lo, mid)
+        assert abs(V.p_eps(n, 1) - lo) / lo < 1e-6
+        assert abs(lo - want) / want < 0.002
+
+
+def test_harness_chain_is_the_instruction_chain():
+    """The validation harness evaluates a k-element vector set as the chain of k / N_FMA
+    block FMAs; that chain is the oracle's 1 x 1 x k tile GEMM with instruction K = k."""
+    import validate_algorithm3 as V
+    for preset, fmt, k in (("cdna3_fp16", "fp16", 16), ("cdna3_xf32", "xf32", 8)):
+        spec = PRESETS[preset]
+        a, b, c = W.gen_exp_mantissa(fmt, 200, k, (-14, 15) if fmt == "fp16" else (-126, 63), (-126, 127), seed=0)
+        got = V._chain(lambda s, x, y, z: oracle.block_fma(s, x, y, z), spec, k, a, b, c)
+        for v in range(0, 200, 7):
+            want = oracle.gemm_entries(spec, k, k, a[v:v + 1], b[v:v + 1], c[v:v + 1].reshape(1, 1), [0], [0])[0]
+            assert got[v] == want, (preset, v)
+
+
+# ---------------------------------------------------------------------------
+# fp16 output (Table 3's note: NVIDIA fp16 and fp8 inputs with fp16 c and d)
+# ---------------------------------------------------------------------------
+def test_round_fp16_is_numpy_binary16():
+    """The closed-form binary16 rounding used below agrees with numpy's binary64 ->
+    binary16 conversion (IEEE RNE) on values binary64 holds exactly, subnormals and
+    overflow included."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal(20000) * np.exp2(rng.integers(-30, 18, 20000))
+    x[:50] = [65504.0, 65519.99, 65520.0, 2.0 ** -24, 2.0 ** -25, 2.0 ** -25 * 1.0001, 3 * 2.0 ** -26,
+              -2.0 ** -14, 2.0 ** -14 - 2.0 ** -25, 1e-9] + list(rng.standard_normal(40) * 2.0 ** -20)
+    with np.errstate(over="ignore"):
+        want16 = x.astype(np.float16).view(np.uint16)
+    for v, want in zip(x, want16.tolist()):
+        assert exact_spec.round_fp16(Fraction(float(v))) == want, v
+
+
+@pytest.mark.parametrize("fmt,k", [("fp16", 4), ("fp16", 16), ("e4m3", 8), ("e5m2", 8)])
+@pytest.mark.parametrize("mode", ["rne", "rtz"])
+def test_fp16_output_exact_model_is_correctly_rounded(fmt, k, mode):
+    a, b, _ = W.gen_block_fma_set(fmt, 1500, k, seed=40 + k, special_rate=0.02)
+    c = W.independent_bits(np.random.default_rng(41), "fp16", (1500,), "ocp", 0.02).astype(np.uint32)
+    spec = dict(fmt_a=fmt, fmt_b=fmt, arch="exact", n_fma=k, out_round=mode, acc_fmt="fp16", nan_bits=0x7E00)
+    d = oracle.block_fma(spec, a, b, c)
+    for v in range(len(c)):
+        want = exact_spec.exact_block(fmt, a[v], b[v], c[v], mode, nan_bits=0x7E00, acc="fp16")
+        assert d[v] == want, (fmt, v, a[v], b[v], hex(c[v]), hex(d[v]), hex(want))
+
+
+def test_fp16_output_wide_alignment_equals_exact_rtz():
+    """Early-c global alignment keeping more fraction bits than the exponent spread of
+    the terms is the exact sum rounded toward zero to binary16."""
+    a, b, _ = W.gen_exp_mantissa("fp16", 3000, 8, (-6, 6), (-14, 15), seed=0)
+    c = W.gen_exp_mantissa("fp16", 3000, 1, (-8, 8), (-14, 15), seed=1)[0].reshape(-1).astype(np.uint32)
+    spec = dict(PRESETS["b200_fp16_f16"], n_fma=8, align_frac=60, emin_lim=None)
+    d = oracle.block_fma(spec, a, b, c)
+    for v in range(len(c)):
+        assert d[v] == exact_spec.exact_block("fp16", a[v], b[v], c[v], "rtz", nan_bits=0x7E00, acc="fp16"), v
+
+
+def test_fp16_output_hand_traced():
+    """B200 fp16-output model (F_p = 25, e_min^lim = -21, RTZ, c = 0 discarded):
+      p1 = 2^-12 * 2^-12 = 2^-24 (e = -24), p2 = -2^-23 * 2^-24 = -2^-47 (e = -28).
+      e_max = max(-24, -28, -21) = -21, grid 2^-46: p2 truncates to 0, the sum is 2^-24,
+      the smallest binary16 subnormal (0x0001).  Without the limit e_max = -24, the grid
+      2^-49 keeps p2, and 2^-24 - 2^-47 rounds toward zero to 0; so does the exact sum.
+    Overflow: 65504 * 2 gives 0x7BFF (RTZ) and 0x7C00 (RNE); an Inf operand gives
+    0x7C00; Inf - Inf the binary16 NaN."""
+    spec = PRESETS["b200_fp16_f16"]
+    e16 = lambda x: encode_exact(parse_value(x), "fp16")
+    k = spec["n_fma"]
+
+    def run(s, av, bv, cbits=0):
+        a = np.array([[e16(x) for x in av] + [0] * (k - len(av))], np.uint16)
+        b = np.array([[e16(x) for x in bv] + [0] * (k - len(bv))], np.uint16)
+        return int(oracle.block_fma(s, a, b, np.array([cbits], np.uint32))[0])
+
+    assert run(spec, ["2^-12", "-2^-23"], ["2^-12", "2^-24"]) == 0x0001
+    assert run(dict(spec, emin_lim=None), ["2^-12", "-2^-23"], ["2^-12", "2^-24"]) == 0x0000
+    assert run(dict(spec, arch="exact"), ["2^-12", "-2^-23"], ["2^-12", "2^-24"]) == 0x0000
+    assert run(spec, ["65504"], ["2"]) == 0x7BFF
+    assert run(dict(spec, out_round="rne"), ["65504"], ["2"]) == 0x7C00
+    assert run(spec, ["inf"], ["2"]) == 0x7C00
+    assert run(spec, ["inf", "-inf"], ["1", "1"]) == 0x7E00
+    assert run(spec, ["1"], ["1"], e16("-1")) == 0x0000            # exact cancellation: +0
+    k = 1
+    assert run(dict(spec, n_fma=1), ["-0"], ["1"], 0x8000) == 0x8000   # -0 * 1 + -0
+    assert run(dict(spec, n_fma=1), ["-0"], ["1"], 0x0000) == 0x0000   # -0 * 1 + +0
+
+
+def test_fp16_output_chain_carries_binary16():
+    """A GEMM chain with the fp16 accumulator: each block's binary16 result is the next
+    block's addend (oracle GEMM = repeated block FMAs)."""
+    spec = PRESETS["a100_fp16_f16"]
+    a, b, _ = W.gen_exp_mantissa("fp16", 60, 32, (-8, 8), (-14, 15), seed=2)
+    c = W.gen_exp_mantissa("fp16", 60, 1, (-4, 4), (-14, 15), seed=3)[0].reshape(-1).astype(np.uint32)
+    d = c.copy()
+    for j in range(0, 32, spec["n_fma"]):
+        d = oracle.block_fma(spec, np.ascontiguousarray(a[:, j:j + 8]), np.ascontiguousarray(b[:, j:j + 8]), d)
+    for v in range(60):
+        want = oracle.gemm_entries(spec, 32, 16, a[v:v + 1], b[v:v + 1], c[v:v + 1].reshape(1, 1), [0], [0])[0]
+        assert want == d[v] and d[v] <= 0xFFFF
