@@ -426,6 +426,30 @@ def test_empty_single_and_ragged(L):
         assert np.array_equal(got, oracle.block_fma(spec, a, b, c))
 
 
+@pytest.mark.parametrize("fmt,k", [("fp16", 4), ("bf16", 4), ("xf32", 2)])
+@pytest.mark.parametrize("name", ["ga_trunc", "ga_rne"])
+def test_paired_sets_tails_and_alignment(L, fmt, k, name):
+    """Global alignment on 8-byte sets runs two sets per thread with 16-byte loads: odd
+    counts end with a one-set launch, and operands only 8-byte aligned (or c, d only
+    4-byte aligned) take the one-set kernel; every case against the oracle."""
+    spec = block_models(fmt, k)[name]
+    m = L.Model(spec)
+    for n in (2, 3, 63, 64, 65, 100001):
+        a, b, c = W.gen_block_fma_set(fmt, n, k, seed=n + 5)
+        want = oracle.block_fma(spec, a, b, c)
+        for off_ab, off_cd in ((0, 0), (8, 0), (0, 4)):
+            def place(x, off):
+                raw = np.ascontiguousarray(x).view(np.uint8).reshape(-1)
+                buf = torch.zeros(raw.size + 64, dtype=torch.uint8, device="cuda")
+                buf[off:off + raw.size] = torch.from_numpy(raw).cuda()
+                return buf[off:off + raw.size]
+            da, db = place(a, off_ab), place(b, off_ab)
+            dc = place(c, off_cd).view(torch.int32)                      # n elements, 4-byte aligned
+            dd = place(np.zeros(n, np.uint32), off_cd).view(torch.int32)
+            L.block_fma(m, da, db, dc, dd)
+            got = dd.cpu().numpy().view(np.uint32)
+            assert np.array_equal(got, want), f"{fmt} {name} n={n} offsets {off_ab}/{off_cd}\n" + mismatches(got, want)
+
 @pytest.mark.parametrize("pinned", [True, False])
 def test_host_entry_point(L, pinned):
     """mcemu_block_fma_host on page-locked buffers (read in place by the kernel) and on
