@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include "core.cuh"
+#include "stream_pair.cuh"
 
 namespace mcemu {
 
@@ -305,6 +306,84 @@ __device__ __forceinline__ bool f8_exact_fp32(const DevModel &m, const uint32_t 
   return exact_fp32_sum<K>(p, cb, m.rne, m.nan_bits, r) == 0;
 }
 
+// FP8 K=8 sets (8 bytes per operand set) through the paired kernel of stream_pair.cuh:
+// early-c global alignment through the product table with special values in line, and
+// OCP exact-then-round on the FP32 pipe with the undecided sets (ties that the error
+// bound leaves open) batched per warp for the integer path.
+template <int ID, int RM> struct F8GaPairEv {
+  static constexpr bool kSlowQueue = false, kTable = true;
+  static constexpr size_t kTableBytes = sizeof(F8Table);
+  static constexpr int kThreads = 512;           // the table lookups want two 512-thread CTAs per SM
+  static __device__ __forceinline__ const void *table() { return f8_table<ID>().v; }
+  static __device__ __forceinline__ uint32_t eval(const DevModel &m, const GaPairK &k, const uint16_t *tab,
+                                                  const uint32_t (&wa)[2], const uint32_t (&wb)[2], uint32_t cb,
+                                                  uint32_t &flag) {
+    flag = 0u;
+    return f8_eval<MCEMU_ARCH_GA_EARLY, ID, 8, RM != 0>(m, PipeConsts{(uint32_t)k.m1, k.p24, k.p22}, tab, wa, wb, cb);
+  }
+  static __device__ __forceinline__ uint32_t special(const DevModel &m, const uint32_t (&wa)[2],
+                                                     const uint32_t (&wb)[2], uint32_t cb) {
+    return pair_general<MCEMU_ARCH_GA_EARLY, ID, RM>(m, wa, wb, cb);
+  }
+  static __device__ __forceinline__ uint32_t general(const DevModel &m, const uint32_t (&wa)[2],
+                                                     const uint32_t (&wb)[2], uint32_t cb) {
+    return pair_general<MCEMU_ARCH_GA_EARLY, ID, RM>(m, wa, wb, cb);
+  }
+};
+
+template <int ID, int RM> struct F8ExactPairEv {
+  static constexpr bool kSlowQueue = true, kTable = false;
+  static constexpr size_t kTableBytes = 0;
+  static constexpr int kThreads = kPairThreads;
+  static __device__ __forceinline__ const void *table() { return nullptr; }
+  static __device__ __forceinline__ uint32_t eval(const DevModel &m, const GaPairK &, const uint16_t *,
+                                                  const uint32_t (&wa)[2], const uint32_t (&wb)[2], uint32_t cb,
+                                                  uint32_t &flag) {
+    uint32_t r = 0u;
+    flag = f8_exact_fp32<ID, 8>(m, wa, wb, cb, r) ? 0u : 2u;
+    return r;
+  }
+  static __device__ __forceinline__ uint32_t special(const DevModel &m, const uint32_t (&wa)[2],
+                                                     const uint32_t (&wb)[2], uint32_t cb) {
+    return pair_general<MCEMU_ARCH_EXACT, ID, RM>(m, wa, wb, cb);
+  }
+  static __device__ __forceinline__ uint32_t general(const DevModel &m, const uint32_t (&wa)[2],
+                                                     const uint32_t (&wb)[2], uint32_t cb) {
+    return pair_general<MCEMU_ARCH_EXACT, ID, RM>(m, wa, wb, cb);
+  }
+};
+
+template <class Ev>
+static int f8_run_pair(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c, uint32_t *d,
+                       cudaStream_t s) {
+  auto kern = pair_kernel<Ev>;
+  const int shm = Ev::kTable ? (int)Ev::kTableBytes : 0;
+  if (shm && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, shm) != cudaSuccess)
+    return MCEMU_ERR_CUDA;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Ev::kThreads, shm);
+  if (per_sm < 1) per_sm = 1;
+  const size_t np = n / 2, want = (np + Ev::kThreads - 1) / Ev::kThreads, full = (size_t)sms * per_sm;
+  const int grid = (int)(want < full ? want : full);
+  const GaPairK k{m.p0mul, m.p0cmul, 0, 1u, 2u, 1u << 16, 0u, 1u << 9, 1u << 23, -1, -2, 1u << 24, 1u << 22};
+  kern<<<grid, Ev::kThreads, shm, s>>>(m, (uint32_t)np, (const uint4 *)a, (const uint4 *)b, (const uint2 *)c,
+                                       (uint2 *)d, k);
+  return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
+}
+
+// The paired kernel takes OCP exact-then-round at K = 8 (the FP32-pipe evaluation) with
+// 16-byte-aligned operands and 8-byte-aligned c, d.  Global alignment keeps f8_kernel:
+// its product-table lookups want the occupancy of 512-thread CTAs (measured 5-7 %
+// slower in the paired kernel).
+template <int ID>
+static bool f8_pair_ok(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c, const uint32_t *d) {
+  if (m.k != 8 || n < 2 || n / 2 >= (1u << 31)) return false;
+  if (m.arch == MCEMU_ARCH_EXACT && Fmt<ID>::FNUZ) return false;
+  return ((uintptr_t)a % 16) == 0 && ((uintptr_t)b % 16) == 0 && ((uintptr_t)c % 8) == 0 && ((uintptr_t)d % 8) == 0;
+}
+
 template <int ARCH, int ID, int K, bool RNE>
 __global__ void __launch_bounds__(kF8Threads, 2) f8_kernel(const __grid_constant__ DevModel m, size_t n,
                                                            const uint8_t *__restrict__ a,
@@ -429,6 +508,16 @@ static int f8_run_k(const DevModel &m, size_t n, const void *a, const void *b, c
 template <int ID>
 static int f8_run_id(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c, uint32_t *d,
                      cudaStream_t s) {
+  if (f8_pair_ok<ID>(m, n, a, b, c, d)) {
+    int st;
+    if (m.arch == MCEMU_ARCH_EXACT) st = m.rne ? f8_run_pair<F8ExactPairEv<ID, 1>>(m, n, a, b, c, d, s)
+                                               : f8_run_pair<F8ExactPairEv<ID, 0>>(m, n, a, b, c, d, s);
+    else st = m.rne ? f8_run_pair<F8GaPairEv<ID, 1>>(m, n, a, b, c, d, s)
+                    : f8_run_pair<F8GaPairEv<ID, 0>>(m, n, a, b, c, d, s);
+    if (st != MCEMU_OK || n % 2 == 0) return st;
+    const size_t t = n - 1;                           // the odd last set: the one-set kernel
+    return f8_run_id<ID>(m, 1, (const uint8_t *)a + 8 * t, (const uint8_t *)b + 8 * t, c + t, d + t, s);
+  }
   if (m.arch == MCEMU_ARCH_EXACT) return f8_run_k<MCEMU_ARCH_EXACT, ID, true>(m, n, a, b, c, d, s);
   if (m.rne) return f8_run_k<MCEMU_ARCH_GA_EARLY, ID, true>(m, n, a, b, c, d, s);
   return f8_run_k<MCEMU_ARCH_GA_EARLY, ID, false>(m, n, a, b, c, d, s);

@@ -426,10 +426,10 @@ def test_empty_single_and_ragged(L):
         assert np.array_equal(got, oracle.block_fma(spec, a, b, c))
 
 
-@pytest.mark.parametrize("fmt,k", [("fp16", 4), ("bf16", 4), ("xf32", 2)])
-@pytest.mark.parametrize("name", ["ga_trunc", "ga_rne"])
+@pytest.mark.parametrize("fmt,k", [("fp16", 4), ("bf16", 4), ("xf32", 2), ("e4m3", 8), ("e5m2", 8)])
+@pytest.mark.parametrize("name", ["ga_trunc", "ga_rne", "ieee_exact"])
 def test_paired_sets_tails_and_alignment(L, fmt, k, name):
-    """Global alignment on 8-byte sets runs two sets per thread with 16-byte loads: odd
+    """The models on 8-byte sets run two sets per thread with 16-byte loads: odd
     counts end with a one-set launch, and operands only 8-byte aligned (or c, d only
     4-byte aligned) take the one-set kernel; every case against the oracle."""
     spec = block_models(fmt, k)[name]
