@@ -174,7 +174,7 @@ def run_reference(args, rank):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-STREAM_SOURCES = ("core.cuh", "model.h", "stream.cu", "stream_fp8.cu")
+STREAM_SOURCES = ("core.cuh", "model.h", "stream.cu", "stream_fp8.cu", "stream_pair.cuh")
 
 
 def kernel_source_hash():
@@ -206,7 +206,65 @@ def read_traffic(kernel_key):
     return None
 
 
-def gemm_section(L, torch, dev, steps, parts=("dense", "sparse", "multiword")):
+def c1_launch(L, torch, dev, reps=200):
+    """The 65,536-set FP16 K=4 cancellation workload under global alignment with 3
+    extra bits and truncation: 1.5 MiB of inputs stay in L2, so one launch is short and
+    latency-bound; reported per launch, parity checked in the tests."""
+    a, b, c = W.gen_fp16_cancellation(65536, 4, seed=1)
+    da, db, dc = dev(a), dev(b), dev(c)
+    m = L.Model(L.preset_desc("ga_trunc", "fp16", 4))
+    d = torch.empty(65536, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream()
+    for _ in range(3):
+        L.block_fma(m, da, db, dc, d)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(reps):
+        L.block_fma(m, da, db, dc, d)
+    e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    return {"sets": 65536, "us_per_launch": us, "block_fma_per_s": 65536 / (us * 1e-6),
+            "note": "L2-resident inputs, back-to-back launches"}
+
+
+def int_pipe_peaks(torch):
+    """Measured lane-operation rates of the integer pipes (csrc/peak.cu): lop3 and shf on
+    the ALU pipe, mad.lo on the FMA pipe; the best of three launches each."""
+    import ctypes
+    from bit_exact_emulation_gb300 import build
+    P = ctypes.CDLL(build.build_peak())
+    P.mcpeak_int_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_double)]
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = {}
+    for kind, name in ((0, "alu_lop3"), (1, "alu_shf"), (2, "fma_imad")):
+        best = 0.0
+        for _ in range(3):
+            r = ctypes.c_double(0.0)
+            if P.mcpeak_int_rate(kind, 4096, ctypes.c_void_p(sink.data_ptr()), ctypes.byref(r)) == 0:
+                best = max(best, r.value)
+        out[name] = best
+    out["unit"] = "lane-ops/s"
+    return out
+
+
+# minimum integer work per multiply-accumulate of an emulated GEMM: one significand
+# product, one exponent add, one maximum, one alignment shift, one add (per-block
+# normalisation and rounding on top); the ALU pipe's measured rate is the roof
+OPS_PER_MAC = 5
+
+
+def gemm_roofline(macs_per_s, peaks):
+    if not peaks or not peaks.get("alu_lop3"):
+        return None
+    achieved = macs_per_s * OPS_PER_MAC
+    return {"bound": "alu", "ops_per_mac": OPS_PER_MAC, "achieved": achieved, "peak": peaks["alu_lop3"],
+            "peak_source": "measured (lop3 chains, csrc/peak.cu)", "unit": "lane-ops/s",
+            "frac": achieved / peaks["alu_lop3"]}
+
+
+def gemm_section(L, torch, dev, steps, parts=("dense", "sparse", "multiword"), peaks=None):
     """Time the emulated-GEMM workloads named in `parts`; returns their summary dict."""
     out = {}
     s = torch.cuda.current_stream()
@@ -224,15 +282,15 @@ def gemm_section(L, torch, dev, steps, parts=("dense", "sparse", "multiword")):
 
     # dense BF16 2048^3, 32x32x8 bf16 tile semantics
     if "dense" in parts:
-        out["dense_bf16_2048"] = gemm_dense(L, torch, dev, timed, steps)
+        out["dense_bf16_2048"] = gemm_dense(L, torch, dev, timed, steps, peaks)
     if "sparse" in parts:
-        out["sparse24_e4m3_4096"] = gemm_sparse(L, torch, dev, timed, steps)
+        out["sparse24_e4m3_4096"] = gemm_sparse(L, torch, dev, timed, steps, peaks)
     if "multiword" in parts:
-        out["multiword_fp64_4096"] = gemm_multiword(L, torch, timed, steps)
+        out["multiword_fp64_4096"] = gemm_multiword(L, torch, timed, steps, peaks)
     return out
 
 
-def gemm_dense(L, torch, dev, timed, steps):
+def gemm_dense(L, torch, dev, timed, steps, peaks=None):
     M = N = K = 2048
     A, Bt, C = W.gen_dense_bf16(M, N, K, seed=3)
     dA, dB, dC = dev(A), dev(Bt), dev(C)
@@ -243,11 +301,12 @@ def gemm_dense(L, torch, dev, timed, steps):
         m = L.Model(desc)
         D = torch.empty((M, N), dtype=torch.int32, device="cuda")
         sec = timed(lambda: L.tile_gemm(m, t, dA, dB, dC, D), steps)
-        dense[name] = {"ms": sec * 1e3, "gflops": 2.0 * M * N * K / sec / 1e9}
+        dense[name] = {"ms": sec * 1e3, "gflops": 2.0 * M * N * K / sec / 1e9,
+                       "roofline": gemm_roofline(M * N * K / sec, peaks)}
     return dense
 
 
-def gemm_sparse(L, torch, dev, timed, steps):
+def gemm_sparse(L, torch, dev, timed, steps, peaks=None):
     """2:4 sparse E4M3 4096^3, 16x16x32 tile semantics."""
     M = N = K = 4096
     A, Bt, C = W.gen_sparse_e4m3(M, N, K, seed=4)
@@ -262,11 +321,12 @@ def gemm_sparse(L, torch, dev, timed, steps):
         D = torch.empty((M, N), dtype=torch.int32, device="cuda")
         sec = timed(lambda: L.sparse24_gemm(m, ts, Ac, meta, dB, dC, D), steps)
         sparse[name] = {"ms": sec * 1e3, "gflops_effective": 2.0 * M * N * (K // 2) / sec / 1e9,
-                        "gflops_dense_equivalent": 2.0 * M * N * K / sec / 1e9}
+                        "gflops_dense_equivalent": 2.0 * M * N * K / sec / 1e9,
+                        "roofline": gemm_roofline(M * N * (K // 2) / sec, peaks)}
     return sparse
 
 
-def gemm_multiword(L, torch, timed, steps):
+def gemm_multiword(L, torch, timed, steps, peaks=None):
     """Multi-word FP64 4096^3: 3 BF16 words, 9 and 6 word products, CDNA3 BF16 word model."""
     M = N = K = 4096
     t = L.tile(0, 32, 32, 8, 4)
@@ -288,10 +348,54 @@ def gemm_multiword(L, torch, timed, steps):
         Dh = D.cpu().numpy()
         rel = [abs(Fraction(float(Dh[i, j])) - x) / abs(x) for (i, j), x in zip(zip(si, sj), exact) if x != 0]
         mw[label] = {"ms": sec * 1e3, "gflops_emulated": npairs * 2.0 * M * N * K / sec / 1e9,
+                     "roofline": gemm_roofline(npairs * M * N * K / sec, peaks),
                      "rel_fro_error": float(np.sqrt(e2 / r2)),
                      "rel_err_exact_sampled": {"max": float(max(rel)), "median": float(np.median([float(r) for r in rel])),
                                                "entries": len(rel)}}
     return mw
+
+
+def oracle_gemm_sample(fn, M, N, entries, gpu_ms):
+    """The oracle on `entries` sampled outputs of a GEMM, single host thread: its time per
+    output, and the whole GEMM extrapolated from it (labelled as such)."""
+    rng = np.random.default_rng(17)
+    ii = rng.integers(0, M, entries).astype(np.int32)
+    jj = rng.integers(0, N, entries).astype(np.int32)
+    t0 = time.perf_counter()
+    fn(ii, jj)
+    dt = time.perf_counter() - t0
+    per = dt / entries
+    return {"entries": entries, "threads": 1, "s_per_output": per,
+            "whole_gemm_s_extrapolated": per * M * N, "gpu_speedup_extrapolated": per * M * N / (gpu_ms / 1e3)}
+
+
+def cpu_gemm_baseline(gemm):
+    """CPU-baseline leg for the GEMM workloads: the oracle on sampled outputs of each
+    (the inputs regenerated from their seeds), one host thread."""
+    import oracle
+    from oracle.presets import PRESETS, block_models
+    out = {}
+    if "dense_bf16_2048" in gemm:
+        M = N = K = 2048
+        A, Bt, C = W.gen_dense_bf16(M, N, K, seed=3)
+        out["dense_bf16_2048 cdna3_bf16"] = oracle_gemm_sample(
+            lambda ii, jj: oracle.gemm_entries(PRESETS["cdna3_bf16"], K, 8, A, Bt, C, ii, jj), M, N, 64,
+            gemm["dense_bf16_2048"]["cdna3_bf16"]["ms"])
+    if "sparse24_e4m3_4096" in gemm:
+        M = N = K = 4096
+        A, Bt, C = W.gen_sparse_e4m3(M, N, K, seed=4)
+        Ac, meta, _ = oracle.sparse24_compress("e4m3", A)
+        spec = block_models("e4m3", 8)["ga_trunc"]
+        out["sparse24_e4m3_4096 ga_trunc"] = oracle_gemm_sample(
+            lambda ii, jj: oracle.sparse24_entries(spec, K, 32, Ac, meta, Bt, C, ii, jj), M, N, 32,
+            gemm["sparse24_e4m3_4096"]["ga_trunc"]["ms"])
+    if "multiword_fp64_4096" in gemm:
+        M = N = K = 4096
+        A, Bt = W.gen_multiword_fp64(M, N, K, seed=5)
+        out["multiword_fp64_4096 9_products"] = oracle_gemm_sample(
+            lambda ii, jj: oracle.multiword_entries(PRESETS["cdna3_bf16"], 8, 3, False, A, Bt, ii, jj), M, N, 4,
+            gemm["multiword_fp64_4096"]["9_products"]["ms"])
+    return out
 
 
 def exact_dot(x, y):
@@ -465,9 +569,11 @@ def main():
             if not np.array_equal(outs[li].numpy().view(np.uint32), outputs[(fmt, name)]):
                 e2e["mismatch"] = f"{fmt} {name}"
 
+    peaks = int_pipe_peaks(torch) if rank == 0 else None
+    c1 = c1_launch(L, torch, dev) if rank == 0 else None
     gemm = None
     if rank == 0 and not args.no_gemm:
-        gemm = gemm_section(L, torch, dev, max(1, min(args.steps, 3)), tuple(args.gemm_parts.split(",")))
+        gemm = gemm_section(L, torch, dev, max(1, min(args.steps, 3)), tuple(args.gemm_parts.split(",")), peaks)
 
     if world > 1:
         dist.barrier()
@@ -476,15 +582,20 @@ def main():
     threads = os.cpu_count() or 1
     per_combo = min(100_000, n_vec // 2)
     n_cpu, t_cpu, mism = cpu_baseline(data, outputs, per_combo, threads)
+    n_1, t_1, _ = cpu_baseline(data, {}, min(10_000, per_combo), 1)
     cpu = {"value": n_cpu / t_cpu, "unit": "block-FMA/s", "cores": threads, "kind": "oracle",
            "sample": f"{per_combo} seeded vector sets of each (format, model) pair of the step, "
-                     f"{n_cpu} block FMAs; the same sample checks the GPU outputs"}
+                     f"{n_cpu} block FMAs; the same sample checks the GPU outputs",
+           "single_thread": {"value": n_1 / t_1, "unit": "block-FMA/s", "cores": 1,
+                             "sample": f"{min(10_000, per_combo)} sets of each pair"}}
+    if gemm:
+        cpu["gemm_sampled_outputs"] = cpu_gemm_baseline(gemm)
     line = {"metric": METRIC, "value": value, "unit": "block-FMA/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int32/int64 integer significand arithmetic", "data": "synthetic",
+            "vs_baseline": None, "dtype": "bit-exact: integer significands and error-free fp32 sums", "data": "synthetic",
             "config": dict(workload_config(n_vec), parity_sample_mismatches=mism, parity_sample=n_cpu),
             "gpu_launches": len(launches) * args.steps, "clocks": clk, "roofline": roofline,
-            "cpu_baseline": cpu, "e2e": e2e, "gemm": gemm}
+            "cpu_baseline": cpu, "e2e": e2e, "int_pipe_peaks": peaks, "c1_fp16_cancellation": c1, "gemm": gemm}
     print(json.dumps(line), flush=True)
 
 

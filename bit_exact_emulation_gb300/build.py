@@ -37,6 +37,7 @@ def up_to_date() -> bool:
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if not force and up_to_date():
+        build_peak()
         return LIB_PATH
     nvcc = _nvcc()
     objdir = os.path.join(HERE, "_build")
@@ -60,7 +61,25 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
+    build_peak()
     return LIB_PATH
+
+
+PEAK_PATH = os.path.join(HERE, "libmcpeak.so")
+
+
+def build_peak() -> str:
+    """The pipe-peak microbenchmark (csrc/peak.cu) that the benchmark uses for its
+    integer rooflines; a library of its own, not part of the emulator."""
+    src = os.path.join(CSRC, "peak.cu")
+    if os.path.exists(PEAK_PATH) and os.path.getmtime(PEAK_PATH) >= os.path.getmtime(src):
+        return PEAK_PATH
+    tmp = PEAK_PATH + f".tmp{os.getpid()}"
+    r = subprocess.run([_nvcc(), *ARCH, *FLAGS, "-shared", "-o", tmp, src, "-lcudart"], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on peak.cu:\n{r.stderr}")
+    os.replace(tmp, PEAK_PATH)
+    return PEAK_PATH
 
 
 if __name__ == "__main__":
