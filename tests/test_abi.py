@@ -143,3 +143,22 @@ def test_swmmac_src_layout_matches_oracle(L):
         for idx in range(16):
             for k in range(kmax):
                 assert L.swmmac_src_layout(op, idx, k) == oracle.swmmac_src_pos(op, idx, k)
+
+
+def test_static_scratch_entry_without_a_device(L):
+    """On a host without a GPU the no-allocation multi-word entry point's first call
+    (the per-device lookup of its scratch array) returns MCEMU_ERR_CUDA; nothing is
+    launched.  Skipped where a GPU is present (these are host buffers)."""
+    import numpy as np
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    m = L.Model(PRESETS["cdna3_bf16"])
+    A = np.zeros((4, 8))
+    B = np.zeros((4, 8))
+    D = np.zeros((4, 4))
+    t = L.tile(0, 32, 32, 8, 4)
+    p = lambda x: ctypes.c_void_p(x.ctypes.data)
+    st = L.lib().mcemu_multiword_gemm_static(m.handle, ctypes.byref(t), 3, 0, 4, 4, 8, p(A), 8, p(B), 8, p(D), 4,
+                                             None)
+    assert st == 5                               # MCEMU_ERR_CUDA

@@ -32,11 +32,17 @@ CASES = [  # word model, words, truncated product set, M, N, K
     ("cdna3_bf16", 3, False, 64, 48, 256),
     ("ga_trunc", 3, True, 37, 29, 100),
     ("cdna3_bf16", 2, False, 5, 130, 72),
+    # a word model the per-pair fast GEMM does not take (exact-then-round): the words
+    # go through the fused general kernel, which also reads the fixed scratch
+    ("ieee_exact", 3, False, 33, 41, 96),
+    ("ieee_exact", 2, True, 16, 16, 40),
 ]
 
 
 def spec_of(name):
-    return PRESETS["cdna3_bf16"] if name == "cdna3_bf16" else block_models("bf16", 8)["ga_trunc"]
+    if name == "cdna3_bf16":
+        return PRESETS["cdna3_bf16"]
+    return block_models("bf16", 8)[name]
 
 
 @pytest.mark.parametrize("case", range(len(CASES)))
