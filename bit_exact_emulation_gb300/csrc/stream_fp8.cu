@@ -124,12 +124,16 @@ template <int ID, int K>
 __device__ __forceinline__ uint32_t f8_special(const DevModel &m, const uint32_t (&e)[K], const uint32_t (&sg)[K],
                                                uint32_t orv, uint32_t cb, uint32_t fnuz_nan) {
   uint32_t s = c_special(cb) | (fnuz_nan || (orv & 0x100u) ? 1u : 0u);
-  if (s == 0u || (s & 6u)) {          // infinite products: their signs matter
-    if (orv & 0x200u) {
+  if constexpr (Fmt<ID>::IEEE) {
+    // E5M2 (OCP) has infinities: the entries' Inf bit (9) under the positive and the
+    // negative sign masks, branch-free (E4M3 and the FNUZ encodings have none)
+    uint32_t pinf = 0u, ninf = 0u;
 #pragma unroll
-      for (int l = 0; l < K; l++)
-        if (e[l] & 0x200u) s |= (sg[l] & 1u) ? 4u : 2u;
+    for (int l = 0; l < K; l++) {
+      pinf |= e[l] & ~sg[l];
+      ninf |= e[l] & sg[l];
     }
+    s |= ((pinf & 0x200u) ? 2u : 0u) | ((ninf & 0x200u) ? 4u : 0u);
   }
   return resolve_special(m, s);
 }
