@@ -450,6 +450,28 @@ def test_paired_sets_tails_and_alignment(L, fmt, k, name):
             got = dd.cpu().numpy().view(np.uint32)
             assert np.array_equal(got, want), f"{fmt} {name} n={n} offsets {off_ab}/{off_cd}\n" + mismatches(got, want)
 
+@pytest.mark.parametrize("fa,fb", [("int8", "int8"), ("uint8", "uint8"), ("int8", "uint8")])
+@pytest.mark.parametrize("sat", [False, True])
+def test_int8_pairs_tails_and_alignment(L, fa, fb, sat):
+    """INT8 K=16 runs two sets per thread: odd counts, and c, d only 4-byte aligned
+    (the one-set kernel), against the integer dot product of the oracle."""
+    spec = dict(fmt_a=fa, fmt_b=fb, arch="exact", n_fma=16, int_saturate=sat)
+    m = L.Model(spec)
+    rng = np.random.default_rng(5)
+    for n in (2, 3, 1001, 65536):
+        a = rng.integers(0, 256, (n, 16), dtype=np.uint64).astype(np.uint8)
+        b = rng.integers(0, 256, (n, 16), dtype=np.uint64).astype(np.uint8)
+        c = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+        c[: n // 3] = 0x7FFFFF00
+        want = oracle.block_fma(spec, a, b, c)
+        for off in (0, 1):                       # c and d 4-byte but not 8-byte aligned: one set per thread
+            bufc = torch.zeros(n + 2, dtype=torch.int32, device="cuda")
+            bufd = torch.zeros(n + 2, dtype=torch.int32, device="cuda")
+            bufc[off:off + n] = torch.from_numpy(c.view(np.int32)).cuda()
+            L.block_fma(m, dev(a), dev(b), bufc[off:off + n], bufd[off:off + n])
+            got = bufd[off:off + n].cpu().numpy().view(np.uint32)
+            assert np.array_equal(got, want), f"{fa}x{fb} sat={sat} n={n} off={off}\n" + mismatches(got, want)
+
 @pytest.mark.parametrize("pinned", [True, False])
 def test_host_entry_point(L, pinned):
     """mcemu_block_fma_host on page-locked buffers (read in place by the kernel) and on
