@@ -189,18 +189,20 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def read_traffic(kernel_key):
-    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+def read_profile_row(kernel_key):
+    """The committed ncu figures of a stream kernel (profiles/traffic.md): DRAM bytes per
+    launch at 10^7 sets, thread instructions per set, ALU-pipe and issue utilisation --
+    when they were taken on the current kernel sources, else None."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
     cur = kernel_source_hash()
     for line in open(path):
         p = [x.strip() for x in line.strip().strip("|").split("|")]
-        if len(p) >= 3 and p[0] == kernel_key and p[2] == cur:
+        if len(p) >= 6 and p[0] == kernel_key and p[-1] == cur:
             try:
-                return float(p[1])
+                return {"traffic": float(p[1]), "inst_per_set": float(p[2]), "alu_pct": float(p[3]),
+                        "issue_pct": float(p[4])}
             except ValueError:
                 return None
     return None
@@ -519,9 +521,13 @@ def main():
     algo_bytes = n_vec * (2 * VEC_BYTES[dfmt] + 8)
     achieved = algo_bytes / (per_launch[dom] / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
+    prof = read_profile_row(f"block_fma {dfmt} {dname}")
     roofline = {"bound": "hbm", "kernel": f"block_fma {dfmt} {dname}", "achieved": achieved, "peak": peak,
                 "peak_source": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": read_traffic(f"block_fma {dfmt} {dname}"),
+                "traffic": prof["traffic"] if prof else None,
+                # the stream kernels are instruction-issue bound: ncu's figures for this kernel (6e6-set capture)
+                "pipes_ncu": ({"inst_per_set": prof["inst_per_set"], "alu_pipe_pct": prof["alu_pct"],
+                               "issue_active_pct": prof["issue_pct"]} if prof else None),
                 "algorithmic_bytes_per_launch": algo_bytes,
                 "per_kernel_gbs": {f"{f} {n}": n_vec * (2 * VEC_BYTES[f] + 8) / (t / 1e3) / 1e9
                                    for (f, n, _, _), t in zip(launches, per_launch)}}
