@@ -276,9 +276,108 @@ template <int ID, int RM> struct GaPairEv {
   }
 };
 
+// Exact-then-round with RNE of one BF16 (K = 4, two elements per word) or truncated
+// XF32 (K = 2) set on the FP32 pipe, every term split against one constant
+// (ExtractScalar of Rump, Ogita and Oishi, "Accurate floating-point summation part I:
+// faithful rounding", SIAM J. Sci. Comput. 31, 2008, Lemma 3.3):
+//  - an element a with exponent field f_a becomes a1 = a 2^(128 - max(f_a, 1)), in
+//    [2, 4) when normal and (0, 2) when subnormal, so p = a1 b1 is exact (8 x 8 or
+//    11 x 11 significand bits) and a b = p 2^(F - 256), F = max(f_a, 1) + max(f_b, 1);
+//  - with M = max(F over the products, max(f_c, 1) + 127) every term is scaled by
+//    2^(256 - M): a product to x = p 2^(F - M), |x| < 16, through a scale that is 0 when
+//    F - M < -126 (the product, below 2^-123, is dropped), and c to x_c = c 2^(256 - M),
+//    |x_c| < 8, by two exact power-of-two multiplies (exponents in [-126, 64]; only a
+//    subnormal x_c, below 2^-126, is rounded);
+//  - with sigma = 2^7 (K = 4) or 2^6 (K = 2), q = fl(sigma + x) - sigma and r = x - q are
+//    exact (x enters through one fused multiply-add each); every q is a multiple of
+//    ulp(sigma) / 2 and |sum q| < sigma, so tau = sum q is exact, and |r| <= ulp(sigma) / 2;
+//  - P = fl(sum r) (K additions) is off from sum r by at most gamma_K (K + 1) ulp(sigma)
+//    / 2 < 2^-36.6 (K = 4) or 2^-39.4 (K = 2) (Higham, Accuracy and Stability of Numerical
+//    Algorithms, Sec. 4.2); with the dropped terms that stays below kBound;
+//  - when |tau| >= |P|, Dekker's Fast2Sum gives t + r = tau + P exactly, so the exact sum
+//    is t + r + d with |d| < kBound, and t is its RNE rounding when |r| + kBound is below
+//    half the spacing of the floats next to t (the smaller one, below |t|).
+// The rounded t goes back by 2^(M - 256) on its exponent field; one at or beyond 2^128
+// is +-Inf.  A zero, tiny (< 2^-124 after scaling), subnormal or undecided result
+// returns 2 (the integer path).  sw is nonzero when an operand or c is Inf or NaN; the
+// result is then meaningless and the caller resolves the set from its classes.
+template <int ID>
+__device__ __forceinline__ int sigma_exact_rn(const uint32_t (&wa)[2], const uint32_t (&wb)[2], uint32_t cb,
+                                              uint32_t &out, uint32_t &sw) {
+  static_assert(ID == F_BF16 || ID == F_XF32T, "BF16 or truncated XF32 elements");
+  constexpr int K = ID == F_BF16 ? 4 : 2;
+  constexpr float kSigma = K == 4 ? 0x1p7f : 0x1p6f;
+  constexpr float kBound = K == 4 ? 0x1p-36f : 0x1p-39f;
+  constexpr uint32_t kE255 = 255u << 23, kE127 = 127u << 23;
+  float p[K];
+  uint32_t F23[K];                                     // F << 23 (F <= 510: fits unsigned)
+  uint32_t top = 0;                                    // the largest exponent field(s) of a and b
+  if constexpr (ID == F_BF16) {
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+      // max(field, 1) << 7 in each 16-bit half; << 16 and the high half's mask put it at 23
+      const uint32_t Ea = vmax2(wa[i] & 0x7F807F80u, 0x00800080u);
+      const uint32_t Eb = vmax2(wb[i] & 0x7F807F80u, 0x00800080u);
+      top = vmax2(top, vmax2(Ea, Eb));
+      const float a_lo = __fmul_rn(__uint_as_float(wa[i] << 16), __uint_as_float(kE255 - (Ea << 16)));
+      const float b_lo = __fmul_rn(__uint_as_float(wb[i] << 16), __uint_as_float(kE255 - (Eb << 16)));
+      const float a_hi = __fmul_rn(__uint_as_float(wa[i] & 0xFFFF0000u), __uint_as_float(kE255 - (Ea & 0xFFFF0000u)));
+      const float b_hi = __fmul_rn(__uint_as_float(wb[i] & 0xFFFF0000u), __uint_as_float(kE255 - (Eb & 0xFFFF0000u)));
+      p[2 * i] = __fmul_rn(a_lo, b_lo);
+      p[2 * i + 1] = __fmul_rn(a_hi, b_hi);
+      const uint32_t Es = Ea + Eb;                     // per half (F << 7) <= 510 << 7: no carry
+      F23[2 * i] = Es << 16;
+      F23[2 * i + 1] = Es & 0xFFFF0000u;
+    }
+    top = (top + 0x00800080u) & 0x80008000u;           // a field of all ones in either half
+  } else {
+#pragma unroll
+    for (int l = 0; l < 2; l++) {
+      const uint32_t xa = wa[l] & 0xFFFFE000u, xb = wb[l] & 0xFFFFE000u;   // 10 mantissa bits
+      const uint32_t Ea = max(xa & 0x7F800000u, 1u << 23), Eb = max(xb & 0x7F800000u, 1u << 23);
+      top = max(top, max(Ea, Eb));
+      p[l] = __fmul_rn(__fmul_rn(__uint_as_float(xa), __uint_as_float(kE255 - Ea)),
+                       __fmul_rn(__uint_as_float(xb), __uint_as_float(kE255 - Eb)));
+      F23[l] = Ea + Eb;
+    }
+    top = top == kE255 ? 1u : 0u;
+  }
+  const uint32_t cf = cb & 0x7F800000u;
+  sw = top | (cf == kE255 ? 1u : 0u);
+  uint32_t M23 = max(cf, 1u << 23) + kE127;
+#pragma unroll
+  for (int l = 0; l < K; l++) M23 = max(M23, F23[l]);
+  // c * 2^k, k = 256 - M in [-252, 128], as 2^k1 2^k2 with k1 = floor(k / 2)
+  const int32_t k23 = (int32_t)(0x80000000u - M23);
+  const int32_t k1 = (k23 >> 1) & (int32_t)0xFF800000;
+  const float xc = __fmul_rn(__fmul_rn(__uint_as_float(cb), __uint_as_float((uint32_t)k1 + kE127)),
+                             __uint_as_float((uint32_t)(k23 - k1) + kE127));
+  float tq = __fadd_rn(__fadd_rn(xc, kSigma), -kSigma);
+  float P = __fadd_rn(xc, -tq);
+#pragma unroll
+  for (int l = 0; l < K; l++) {
+    const float sc = __uint_as_float(kE127 - min(M23 - F23[l], kE127));   // 2^(F - M), 0 below 2^-126
+    const float q = __fadd_rn(__fmaf_rn(p[l], sc, kSigma), -kSigma);
+    tq = __fadd_rn(tq, q);
+    P = __fadd_rn(P, __fmaf_rn(p[l], sc, -q));
+  }
+  const float t = __fadd_rn(tq, P);
+  const float r = __fadd_rn(P, -__fadd_rn(t, -tq));
+  const uint32_t tb = __float_as_uint(t), ta = tb & 0x7FFFFFFFu;
+  const int32_t fr = (int32_t)(ta >> 23) - (k23 >> 23);   // the result's exponent field
+  // 2^e of the float just below |t|: half its spacing is 2^(e - 24)
+  const float h = __uint_as_float((ta - 1u) & 0x7F800000u);
+  out = fr > 254 ? (tb & 0x80000000u) | 0x7F800000u : tb - (uint32_t)k23;
+  const bool ok = fabsf(tq) >= fabsf(P) && ta >= (3u << 23) && fr >= 1 &&
+                  fabsf(r) < __fmaf_rd(h, 0x1p-24f, -kBound);
+  return ok ? 0 : 2;
+}
+
 // Exact-then-round on the FP32 pipe: FP16 with exact fp32 products (special values
-// from the IEEE sum, in line), BF16 and truncated XF32 with rescaled terms (special
-// values queued and resolved from their classes).  A rounding the error bound leaves
+// from the IEEE sum, in line); BF16 and truncated XF32 with RNE through sigma_exact_rn,
+// with RZ through exact_scaled, whose error bound follows the terms (an RZ decision
+// needs the sign of a remainder that can lie far below any fixed bound); special values
+// of those two queued and resolved from their classes.  A rounding the error bound leaves
 // undecided, a subnormal addend or result goes to the integer path, 32 at a time.
 template <int ID, int RM> struct ExactPairEv {
   static constexpr bool kSlowQueue = true, kTable = false;
@@ -298,6 +397,10 @@ template <int ID, int RM> struct ExactPairEv {
         p[2 * i + 1] = __fmul_rn(fa.y, fb.y);
       }
       flag = exact_fp32_sum<4>(p, cb, RM, m.nan_bits, r) ? 2u : 0u;
+    } else if constexpr (RM == 1) {
+      uint32_t sw;
+      const int st = sigma_exact_rn<ID>(wa, wb, cb, r, sw);
+      flag = sw ? 1u : (st ? 2u : 0u);
     } else {
       uint32_t sw = (cb & 0x7F800000u) == 0x7F800000u;
 #pragma unroll
@@ -318,41 +421,53 @@ template <int ID, int RM> struct ExactPairEv {
   }
 };
 
-struct QueuedSet {
-  uint32_t wa0, wa1, wb0, wb1, c, idx;
+// A warp's queue of flagged sets, kept with their data: the four operand words of a set
+// in one 16-byte entry and (c, index) in an 8-byte one, so that a set goes in and out
+// with one vector access of each.
+struct PairQueue {
+  uint4 *ab;
+  uint2 *ci;
 };
 constexpr int kPairQueue = 96;      // entries per warp: fewer than 32 left over plus 64 new ones
 
 // Append the flagged sets of this iteration (at most two per lane) to a warp queue and
 // resolve it 32 entries at a time; qn is warp-uniform.
 template <class Fn>
-__device__ __forceinline__ void pair_enqueue(QueuedSet *q, int &qn, bool s0, bool s1, const uint32_t (&wa0)[2],
-                                             const uint32_t (&wb0)[2], const uint32_t (&wa1)[2],
-                                             const uint32_t (&wb1)[2], uint2 xc, uint32_t p, uint32_t below,
-                                             int lane, uint32_t *d32, Fn resolve) {
+__device__ __forceinline__ void pair_enqueue(PairQueue q, int &qn, bool s0, bool s1, uint4 xa, uint4 xb, uint2 xc,
+                                             uint32_t p, uint32_t below, int lane, uint32_t *d32, Fn resolve) {
   const uint32_t m0 = __ballot_sync(0xFFFFFFFFu, s0), m1 = __ballot_sync(0xFFFFFFFFu, s1);
   if (!(m0 | m1)) return;
-  if (s0) q[qn + __popc(m0 & below)] = QueuedSet{wa0[0], wa0[1], wb0[0], wb0[1], xc.x, 2 * p};
+  if (s0) {
+    const int j = qn + __popc(m0 & below);
+    q.ab[j] = make_uint4(xa.x, xa.y, xb.x, xb.y);
+    q.ci[j] = make_uint2(xc.x, 2 * p);
+  }
   qn += __popc(m0);
-  if (s1) q[qn + __popc(m1 & below)] = QueuedSet{wa1[0], wa1[1], wb1[0], wb1[1], xc.y, 2 * p + 1};
+  if (s1) {
+    const int j = qn + __popc(m1 & below);
+    q.ab[j] = make_uint4(xa.z, xa.w, xb.z, xb.w);
+    q.ci[j] = make_uint2(xc.y, 2 * p + 1);
+  }
   qn += __popc(m1);
   while (qn >= 32) {
     __syncwarp();
-    const QueuedSet e = q[qn - 32 + lane];
-    const uint32_t ua[2] = {e.wa0, e.wa1}, ub[2] = {e.wb0, e.wb1};
-    d32[e.idx] = resolve(ua, ub, e.c);
+    const uint4 e = q.ab[qn - 32 + lane];
+    const uint2 ci = q.ci[qn - 32 + lane];
+    const uint32_t ua[2] = {e.x, e.y}, ub[2] = {e.z, e.w};
+    d32[ci.y] = resolve(ua, ub, ci.x);
     qn -= 32;
     __syncwarp();
   }
 }
 
 template <class Fn>
-__device__ __forceinline__ void pair_drain(const QueuedSet *q, int qn, int lane, uint32_t *d32, Fn resolve) {
+__device__ __forceinline__ void pair_drain(PairQueue q, int qn, int lane, uint32_t *d32, Fn resolve) {
   __syncwarp();
   if (lane < qn) {
-    const QueuedSet e = q[lane];
-    const uint32_t ua[2] = {e.wa0, e.wa1}, ub[2] = {e.wb0, e.wb1};
-    d32[e.idx] = resolve(ua, ub, e.c);
+    const uint4 e = q.ab[lane];
+    const uint2 ci = q.ci[lane];
+    const uint32_t ua[2] = {e.x, e.y}, ub[2] = {e.z, e.w};
+    d32[ci.y] = resolve(ua, ub, ci.x);
   }
 }
 
@@ -371,11 +486,15 @@ __global__ void __launch_bounds__(Ev::kThreads) pair_kernel(const __grid_constan
     __syncthreads();
     tab = reinterpret_cast<const uint16_t *>(pair_table);
   }
-  __shared__ QueuedSet queue[Ev::kThreads / 32][kPairQueue];
-  __shared__ QueuedSet slow_queue[Ev::kSlowQueue ? Ev::kThreads / 32 : 1][kPairQueue];
+  constexpr int kSlowWarps = Ev::kSlowQueue ? Ev::kThreads / 32 : 1;
+  __shared__ uint4 queue_ab[Ev::kThreads / 32][kPairQueue];
+  __shared__ uint2 queue_ci[Ev::kThreads / 32][kPairQueue];
+  __shared__ uint4 slow_ab[kSlowWarps][kPairQueue];
+  __shared__ uint2 slow_ci[kSlowWarps][kPairQueue];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t below = (1u << lane) - 1u;
-  QueuedSet *q = queue[warp], *qs = slow_queue[Ev::kSlowQueue ? warp : 0];
+  const PairQueue q{queue_ab[warp], queue_ci[warp]};
+  const PairQueue qs{slow_ab[Ev::kSlowQueue ? warp : 0], slow_ci[Ev::kSlowQueue ? warp : 0]};
   int qn = 0, qsn = 0;                                          // warp-uniform
   const uint32_t stride = gridDim.x * blockDim.x;
   const uint32_t first = blockIdx.x * blockDim.x + threadIdx.x;
@@ -412,9 +531,9 @@ __global__ void __launch_bounds__(Ev::kThreads) pair_kernel(const __grid_constan
       }
       __stcs(d + p, r);
     }
-    pair_enqueue(q, qn, (f0 & 1u) != 0u, (f1 & 1u) != 0u, wa0, wb0, wa1, wb1, xc, p, below, lane, d32, special);
+    pair_enqueue(q, qn, (f0 & 1u) != 0u, (f1 & 1u) != 0u, xa, xb, xc, p, below, lane, d32, special);
     if constexpr (Ev::kSlowQueue)
-      pair_enqueue(qs, qsn, f0 == 2u, f1 == 2u, wa0, wb0, wa1, wb1, xc, p, below, lane, d32, general);
+      pair_enqueue(qs, qsn, f0 == 2u, f1 == 2u, xa, xb, xc, p, below, lane, d32, general);
   }
   pair_drain(q, qn, lane, d32, special);
   if constexpr (Ev::kSlowQueue) pair_drain(qs, qsn, lane, d32, general);

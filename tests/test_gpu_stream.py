@@ -297,6 +297,71 @@ def test_exact_wide_formats_product_overflow(L, fmt, k, prod_overflow):
         assert np.array_equal(got, want), f"{fmt} {out_round} {prod_overflow}\n" + mismatches(got, want, a, b, c)
 
 
+def _scale_extremes(fmt, n, k, seed):
+    """Sets built from exponent fields at the ends of the range: a product of two
+    largest binades with c anywhere; c in the largest binade with products 120-135
+    binades below it (terms dropped or kept at the scale limit); a subnormal c with
+    the smallest products (the scale of every term rises by up to 2^128); one product
+    on top and the others 120-135 binades below; sums that round up to 2^128."""
+    rng = np.random.default_rng(seed)
+    mb = 7 if fmt == "bf16" else 23
+    dt = np.uint16 if fmt == "bf16" else np.uint32
+
+    def elem(field, size):
+        field = np.clip(field, 0, 254)
+        m = rng.integers(0, 1 << mb, size)
+        if fmt == "xf32":
+            m &= ~((1 << 13) - 1)
+        s = rng.integers(0, 2, size)
+        return ((s << (mb + 8)) | (field << mb) | m).astype(dt)
+
+    fa = rng.integers(1, 255, (n, k))
+    fb = rng.integers(1, 255, (n, k))
+    fc = rng.integers(0, 255, n)
+    mode = rng.integers(0, 5, n)
+    top = mode == 0                                       # products in the top binades
+    fa[top], fb[top] = rng.integers(250, 255, (2, top.sum(), k))
+    big_c = mode == 1                                     # c on top, products far below
+    fc[big_c] = rng.integers(250, 255, big_c.sum())
+    gap = rng.integers(120, 136, (big_c.sum(), k))
+    s = fc[big_c][:, None] + 127 - gap                    # the products' field sums
+    fa[big_c] = np.clip(s // 2, 1, 254)
+    fb[big_c] = np.clip(s - fa[big_c], 1, 254)
+    sub_c = mode == 2                                     # subnormal c, tiny products
+    fc[sub_c] = 0
+    fa[sub_c], fb[sub_c] = rng.integers(0, 4, (2, sub_c.sum(), k))
+    spread = mode == 3                                    # one product on top, the rest far below
+    s = rng.integers(200, 400, spread.sum())[:, None] - np.concatenate(
+        [np.zeros((spread.sum(), 1), np.int64), rng.integers(120, 136, (spread.sum(), k - 1))], 1)
+    fa[spread] = np.clip(s // 2, 1, 254)
+    fb[spread] = np.clip(s - fa[spread], 1, 254)
+    fc[spread] = rng.integers(0, 100, spread.sum())
+    a, b = elem(fa, (n, k)), elem(fb, (n, k))
+    c = ((rng.integers(0, 2, n) << 31) | (fc << 23) | rng.integers(0, 1 << 23, n)).astype(np.uint32)
+    ovf = np.flatnonzero(mode == 4)                       # c = +-max finite plus a product near its ulp
+    c[ovf] = (c[ovf] & 0x80000000) | 0x7F7FFFFF
+    a[ovf], b[ovf] = elem(rng.integers(120, 128, (ovf.size, k)), (ovf.size, k)), elem(
+        rng.integers(230, 250, (ovf.size, k)), (ovf.size, k))
+    cancel = np.flatnonzero(top & (rng.random(n) < 0.5))  # the top product cancelled exactly
+    for l in range(0, k, 2):
+        a[cancel, l + 1] = a[cancel, l]
+        b[cancel, l + 1] = b[cancel, l] ^ dt(1 << (mb + 8))
+    b[cancel, k - 1] ^= dt(rng.integers(0, 2) << 4)      # one pair left slightly off
+    return a, b, c
+
+
+@pytest.mark.parametrize("fmt,k", [("bf16", 4), ("xf32", 2)])
+def test_exact_scale_extremes(L, fmt, k):
+    """Exact-then-round, RNE and RTZ, on BF16/XF32 sets at the ends of the exponent range,
+    where the terms' common rescaling, its limits and the dropped terms decide the result."""
+    a, b, c = _scale_extremes(fmt, 60000, k, seed=83)
+    for out_round in ("rne", "rtz"):
+        spec = dict(block_models(fmt, k)["ieee_exact"], out_round=out_round)
+        got = gpu_block(L, spec, a, b, c)
+        want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+        assert np.array_equal(got, want), f"{fmt} {out_round}\n" + mismatches(got, want, a, b, c)
+
+
 F16_OUT = ["b200_fp16_f16", "h100_fp16_f16", "a100_fp16_f16", "b200_fp8_f16", "h100_fp8_f16"]
 
 
