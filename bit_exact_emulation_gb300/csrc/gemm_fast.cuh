@@ -85,6 +85,42 @@ __device__ __forceinline__ void stage_chunk(const DevModel &m, int bshift, int i
   }
 }
 
+// The gather form of the 2:4-sparse GEMM (SPARSE = 2): a chunk holds KCA compressed
+// terms of A (compressed k0c .. k0c + kcc) and the 2 KCA dense rows of B^T they draw on.
+// Compressed term q of row r goes to [q][r] as (S, E, sign) plus, in aI, the offset of
+// its B row in the panel, (4 (q / 2) + idx) * kFS with idx the metadata index of its
+// group (k0c is even, so a chunk starts on a group).  A row with invalid metadata
+// (idx0 >= idx1) or an Inf/NaN, and a column of B with an Inf/NaN, are flagged.
+template <int ESZ>
+__device__ __forceinline__ void stage_chunk_gather(const DevModel &m, int bshift, int i0, int j0, int k0c, int kcc,
+                                                   int KCA, int M, int N, const uint8_t *__restrict__ Ac, int64_t ldac,
+                                                   const uint8_t *__restrict__ meta, int64_t ldm,
+                                                   const uint8_t *__restrict__ Bt, int64_t ldb, int32_t *aS,
+                                                   int32_t *aE, int32_t *aG, int32_t *aI, int32_t *bS, int32_t *bE,
+                                                   int32_t *bG, uint8_t *aSpec, uint8_t *bSpec) {
+  for (int e = threadIdx.x; e < kFB * KCA; e += blockDim.x) {
+    const int r = e / KCA, q = e % KCA;
+    int32_t S = 0, E = kZeroE, G = 1, I = 0;
+    if (i0 + r < M && q < kcc) {
+      const int kq = k0c + q;
+      const uint32_t mb = meta[(int64_t)(i0 + r) * ldm + (kq >> 1)];
+      const uint32_t idx0 = mb & 3u, idx1 = (mb >> 2) & 3u;
+      if (idx0 >= idx1) aSpec[r] = 1;                    // not a valid 2:4 pattern
+      I = (4 * (q >> 1) + (int)((kq & 1) ? idx1 : idx0)) * kFS;
+      if (stage_elem(m.fa, fld<ESZ>(Ac, (int64_t)(i0 + r) * ldac + kq), S, E, G)) aSpec[r] = 1;
+    }
+    aS[q * kFS + r] = S; aE[q * kFS + r] = E; aG[q * kFS + r] = G; aI[q * kFS + r] = I;
+  }
+  const int KB = 2 * KCA, kb = 2 * kcc, k0 = 2 * k0c;
+  for (int e = threadIdx.x; e < kFB * KB; e += blockDim.x) {
+    const int r = e / KB, q = e % KB;
+    int32_t S = 0, E = kZeroE, G = 1;
+    if (j0 + r < N && q < kb && stage_elem(m.fb, fld<ESZ>(Bt, (int64_t)(j0 + r) * ldb + k0 + q), S, E, G))
+      bSpec[r] = 1;
+    bS[q * kFS + r] = S << bshift; bE[q * kFS + r] = E; bG[q * kFS + r] = G;
+  }
+}
+
 // The whole chain of one output with the general evaluator, reading raw operands
 // from global memory (outputs that met a case the fast path leaves out); C == nullptr
 // stands for C = 0.
@@ -177,9 +213,12 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_early_kernel(const __grid_c
                                                                 int64_t ldb, const uint32_t *C, int64_t ldc,
                                                                 uint32_t *D, int64_t ldd) {
   extern __shared__ int32_t fsm[];
-  const int KC = fast_chunk(kt);
-  int32_t *aS = fsm, *aE = aS + KC * kFS, *aG = aE + KC * kFS;         // [KC][kFS]
-  int32_t *bS = aG + KC * kFS, *bE = bS + KC * kFS, *bG = bE + KC * kFS;  // B significands << P0
+  constexpr bool GATHER = SPARSE == 2;
+  const int KC = fast_chunk(kt);                                         // dense positions per chunk
+  const int KCA = GATHER ? KC / 2 : KC;                                  // A panel rows
+  int32_t *aS = fsm, *aE = aS + KCA * kFS, *aG = aE + KCA * kFS;        // [KCA][kFS]
+  int32_t *aI = aG + KCA * kFS;                                          // gather: B row offsets
+  int32_t *bS = aI + (GATHER ? KCA * kFS : 0), *bE = bS + KC * kFS, *bG = bE + KC * kFS;  // B significands << P0
   uint8_t *aSpec = reinterpret_cast<uint8_t *>(bG + KC * kFS);          // [kFB] per row
   uint8_t *bSpec = aSpec + kFB;
   const int i0 = blockIdx.y * kFB, j0 = blockIdx.x * kFB;
@@ -218,8 +257,12 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_early_kernel(const __grid_c
     __syncthreads();
     if (tid < kFB) { aSpec[tid] = 0; bSpec[tid] = 0; }
     __syncthreads();
-    stage_chunk<ESZ, SPARSE>(m, m.P0, i0, j0, k0, kc, KC, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, bS, bE, bG,
-                             aSpec, bSpec);
+    if constexpr (GATHER)
+      stage_chunk_gather<ESZ>(m, m.P0, i0, j0, k0 / 2, kc / 2, KCA, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, aI,
+                              bS, bE, bG, aSpec, bSpec);
+    else
+      stage_chunk<ESZ, SPARSE>(m, m.P0, i0, j0, k0, kc, KC, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, bS, bE, bG,
+                               aSpec, bSpec);
     __syncthreads();
     // an Inf/NaN in a row of A or a column of B (or invalid metadata) sends the whole
     // row / column of this thread's tile to the fixup pass
@@ -230,8 +273,10 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_early_kernel(const __grid_c
     for (int b = 0; b < kFT; b++)
       if (bSpec[tj + b]) redo |= 0x1111u << b;
 
-    for (int s0 = 0; s0 < kc; s0 += kt) {
-      const int send = min(s0 + kt, kc);
+    // the chain's units in this chunk: dense positions, or compressed terms (gather)
+    const int ku = GATHER ? kc / 2 : kc, ktu = GATHER ? kt / 2 : kt;
+    for (int s0 = 0; s0 < ku; s0 += ktu) {
+      const int send = min(s0 + ktu, ku);
       for (int b0 = s0; b0 < send; b0 += kblk) {
         const int nt = min(kblk, send - b0);
         // ---- e_max: c's exponent and the limit first, then the products
@@ -248,12 +293,25 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_early_kernel(const __grid_c
           }
         for (int q = b0; q < b0 + nt; q++) {
           const int4 ea = *reinterpret_cast<const int4 *>(aE + q * kFS + ti);
-          const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
-          const int32_t xa[4] = {ea.x, ea.y, ea.z, ea.w}, xb[4] = {eb.x, eb.y, eb.z, eb.w};
+          const int32_t xa[4] = {ea.x, ea.y, ea.z, ea.w};
+          if constexpr (GATHER) {
+            const int4 ia = *reinterpret_cast<const int4 *>(aI + q * kFS + ti);
+            const int32_t ra[4] = {ia.x, ia.y, ia.z, ia.w};
 #pragma unroll
-          for (int a = 0; a < kFT; a++)
+            for (int a = 0; a < kFT; a++) {
+              const int4 eb = *reinterpret_cast<const int4 *>(bE + ra[a] + tj);
+              const int32_t xb[4] = {eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
-            for (int b = 0; b < kFT; b++) em[a][b] = __viaddmax_s32(xa[a], xb[b], em[a][b]);
+              for (int b = 0; b < kFT; b++) em[a][b] = __viaddmax_s32(xa[a], xb[b], em[a][b]);
+            }
+          } else {
+            const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
+            const int32_t xb[4] = {eb.x, eb.y, eb.z, eb.w};
+#pragma unroll
+            for (int a = 0; a < kFT; a++)
+#pragma unroll
+              for (int b = 0; b < kFT; b++) em[a][b] = __viaddmax_s32(xa[a], xb[b], em[a][b]);
+          }
         }
         // ---- the aligned addend starts the sum
         int32_t Sp[kFT][kFT];
@@ -274,20 +332,41 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_early_kernel(const __grid_c
           const int4 sa = *reinterpret_cast<const int4 *>(aS + q * kFS + ti);
           const int4 ea = *reinterpret_cast<const int4 *>(aE + q * kFS + ti);
           const int4 ga = *reinterpret_cast<const int4 *>(aG + q * kFS + ti);
-          const int4 sb = *reinterpret_cast<const int4 *>(bS + q * kFS + tj);
-          const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
-          const int4 gb = *reinterpret_cast<const int4 *>(bG + q * kFS + tj);
           const int32_t SA[4] = {sa.x, sa.y, sa.z, sa.w}, EA[4] = {ea.x, ea.y, ea.z, ea.w}, GA[4] = {ga.x, ga.y, ga.z, ga.w};
-          const int32_t SB[4] = {sb.x, sb.y, sb.z, sb.w}, EB[4] = {eb.x, eb.y, eb.z, eb.w}, GB[4] = {gb.x, gb.y, gb.z, gb.w};
+          if constexpr (GATHER) {
+            // each of the thread's A rows reads B at its own row of the panel
+            const int4 ia = *reinterpret_cast<const int4 *>(aI + q * kFS + ti);
+            const int32_t ra[4] = {ia.x, ia.y, ia.z, ia.w};
 #pragma unroll
-          for (int a = 0; a < kFT; a++)
+            for (int a = 0; a < kFT; a++) {
+              const int4 sb = *reinterpret_cast<const int4 *>(bS + ra[a] + tj);
+              const int4 eb = *reinterpret_cast<const int4 *>(bE + ra[a] + tj);
+              const int4 gb = *reinterpret_cast<const int4 *>(bG + ra[a] + tj);
+              const int32_t SB[4] = {sb.x, sb.y, sb.z, sb.w}, EB[4] = {eb.x, eb.y, eb.z, eb.w};
+              const int32_t GB[4] = {gb.x, gb.y, gb.z, gb.w};
 #pragma unroll
-            for (int b = 0; b < kFT; b++) {
-              const int32_t sh = em[a][b] - EA[a] - EB[b];
-              const uint32_t U = (uint32_t)(SA[a] * SB[b]);
-              const int32_t t = (int32_t)shr32(U, sh);
-              Sp[a][b] += t * (GA[a] * GB[b]);
+              for (int b = 0; b < kFT; b++) {
+                const int32_t sh = em[a][b] - EA[a] - EB[b];
+                const uint32_t U = (uint32_t)(SA[a] * SB[b]);
+                const int32_t t = (int32_t)shr32(U, sh);
+                Sp[a][b] += t * (GA[a] * GB[b]);
+              }
             }
+          } else {
+            const int4 sb = *reinterpret_cast<const int4 *>(bS + q * kFS + tj);
+            const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
+            const int4 gb = *reinterpret_cast<const int4 *>(bG + q * kFS + tj);
+            const int32_t SB[4] = {sb.x, sb.y, sb.z, sb.w}, EB[4] = {eb.x, eb.y, eb.z, eb.w}, GB[4] = {gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+            for (int a = 0; a < kFT; a++)
+#pragma unroll
+              for (int b = 0; b < kFT; b++) {
+                const int32_t sh = em[a][b] - EA[a] - EB[b];
+                const uint32_t U = (uint32_t)(SA[a] * SB[b]);
+                const int32_t t = (int32_t)shr32(U, sh);
+                Sp[a][b] += t * (GA[a] * GB[b]);
+              }
+          }
         }
         // ---- round: the new accumulator (the scale is e_max - F)
         const int32_t gk = m.R0 + F + 127;
@@ -368,9 +447,12 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_late_kernel(const __grid_co
                                                                int64_t ldb, const uint32_t *C, int64_t ldc,
                                                                uint32_t *D, int64_t ldd) {
   extern __shared__ int32_t fsm[];
-  const int KC = fast_chunk(kt);
-  int32_t *aS = fsm, *aE = aS + KC * kFS, *aG = aE + KC * kFS;         // [KC][kFS]
-  int32_t *bS = aG + KC * kFS, *bE = bS + KC * kFS, *bG = bE + KC * kFS;  // B significands << P0
+  constexpr bool GATHER = SPARSE == 2;
+  const int KC = fast_chunk(kt);                                         // dense positions per chunk
+  const int KCA = GATHER ? KC / 2 : KC;                                  // A panel rows
+  int32_t *aS = fsm, *aE = aS + KCA * kFS, *aG = aE + KCA * kFS;        // [KCA][kFS]
+  int32_t *aI = aG + KCA * kFS;                                          // gather: B row offsets
+  int32_t *bS = aI + (GATHER ? KCA * kFS : 0), *bE = bS + KC * kFS, *bG = bE + KC * kFS;  // B significands << P0
   uint8_t *aSpec = reinterpret_cast<uint8_t *>(bG + KC * kFS);          // [kFB] per row
   uint8_t *bSpec = aSpec + kFB;
   const int i0 = blockIdx.y * kFB, j0 = blockIdx.x * kFB;
@@ -406,8 +488,12 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_late_kernel(const __grid_co
     __syncthreads();
     if (tid < kFB) { aSpec[tid] = 0; bSpec[tid] = 0; }
     __syncthreads();
-    stage_chunk<ESZ, SPARSE>(m, m.P0, i0, j0, k0, kc, KC, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, bS, bE, bG,
-                             aSpec, bSpec);
+    if constexpr (GATHER)
+      stage_chunk_gather<ESZ>(m, m.P0, i0, j0, k0 / 2, kc / 2, KCA, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, aI,
+                              bS, bE, bG, aSpec, bSpec);
+    else
+      stage_chunk<ESZ, SPARSE>(m, m.P0, i0, j0, k0, kc, KC, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, bS, bE, bG,
+                               aSpec, bSpec);
     __syncthreads();
 #pragma unroll
     for (int a = 0; a < kFT; a++)
@@ -416,8 +502,10 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_late_kernel(const __grid_co
     for (int b = 0; b < kFT; b++)
       if (bSpec[tj + b]) redo |= 0x1111u << b;
 
-    for (int s0 = 0; s0 < kc; s0 += kt) {
-      const int send = min(s0 + kt, kc);
+    // the chain's units in this chunk: dense positions, or compressed terms (gather)
+    const int ku = GATHER ? kc / 2 : kc, ktu = GATHER ? kt / 2 : kt;
+    for (int s0 = 0; s0 < ku; s0 += ktu) {
+      const int send = min(s0 + ktu, ku);
       for (int b0 = s0; b0 < send; b0 += kblk) {
         const int nt = min(kblk, send - b0);
         // ---- e_max of the products (line 3)
@@ -428,12 +516,25 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_late_kernel(const __grid_co
           for (int b = 0; b < kFT; b++) em[a][b] = kNegE;
         for (int q = b0; q < b0 + nt; q++) {
           const int4 ea = *reinterpret_cast<const int4 *>(aE + q * kFS + ti);
-          const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
-          const int32_t xa[4] = {ea.x, ea.y, ea.z, ea.w}, xb[4] = {eb.x, eb.y, eb.z, eb.w};
+          const int32_t xa[4] = {ea.x, ea.y, ea.z, ea.w};
+          if constexpr (GATHER) {
+            const int4 ia = *reinterpret_cast<const int4 *>(aI + q * kFS + ti);
+            const int32_t ra[4] = {ia.x, ia.y, ia.z, ia.w};
 #pragma unroll
-          for (int a = 0; a < kFT; a++)
+            for (int a = 0; a < kFT; a++) {
+              const int4 eb = *reinterpret_cast<const int4 *>(bE + ra[a] + tj);
+              const int32_t xb[4] = {eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
-            for (int b = 0; b < kFT; b++) em[a][b] = __viaddmax_s32(xa[a], xb[b], em[a][b]);
+              for (int b = 0; b < kFT; b++) em[a][b] = __viaddmax_s32(xa[a], xb[b], em[a][b]);
+            }
+          } else {
+            const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
+            const int32_t xb[4] = {eb.x, eb.y, eb.z, eb.w};
+#pragma unroll
+            for (int a = 0; a < kFT; a++)
+#pragma unroll
+              for (int b = 0; b < kFT; b++) em[a][b] = __viaddmax_s32(xa[a], xb[b], em[a][b]);
+          }
         }
         // ---- aligned, truncated products (line 4)
         int32_t Sp[kFT][kFT];
@@ -448,20 +549,41 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_late_kernel(const __grid_co
           const int4 sa = *reinterpret_cast<const int4 *>(aS + q * kFS + ti);
           const int4 ea = *reinterpret_cast<const int4 *>(aE + q * kFS + ti);
           const int4 ga = *reinterpret_cast<const int4 *>(aG + q * kFS + ti);
-          const int4 sb = *reinterpret_cast<const int4 *>(bS + q * kFS + tj);
-          const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
-          const int4 gb = *reinterpret_cast<const int4 *>(bG + q * kFS + tj);
           const int32_t SA[4] = {sa.x, sa.y, sa.z, sa.w}, EA[4] = {ea.x, ea.y, ea.z, ea.w}, GA[4] = {ga.x, ga.y, ga.z, ga.w};
-          const int32_t SB[4] = {sb.x, sb.y, sb.z, sb.w}, EB[4] = {eb.x, eb.y, eb.z, eb.w}, GB[4] = {gb.x, gb.y, gb.z, gb.w};
+          if constexpr (GATHER) {
+            // each of the thread's A rows reads B at its own row of the panel
+            const int4 ia = *reinterpret_cast<const int4 *>(aI + q * kFS + ti);
+            const int32_t ra[4] = {ia.x, ia.y, ia.z, ia.w};
 #pragma unroll
-          for (int a = 0; a < kFT; a++)
+            for (int a = 0; a < kFT; a++) {
+              const int4 sb = *reinterpret_cast<const int4 *>(bS + ra[a] + tj);
+              const int4 eb = *reinterpret_cast<const int4 *>(bE + ra[a] + tj);
+              const int4 gb = *reinterpret_cast<const int4 *>(bG + ra[a] + tj);
+              const int32_t SB[4] = {sb.x, sb.y, sb.z, sb.w}, EB[4] = {eb.x, eb.y, eb.z, eb.w};
+              const int32_t GB[4] = {gb.x, gb.y, gb.z, gb.w};
 #pragma unroll
-            for (int b = 0; b < kFT; b++) {
-              const int32_t sh = em[a][b] - EA[a] - EB[b];
-              const uint32_t U = (uint32_t)(SA[a] * SB[b]);
-              const int32_t t = (int32_t)shr32(U, sh);
-              Sp[a][b] += t * (GA[a] * GB[b]);
+              for (int b = 0; b < kFT; b++) {
+                const int32_t sh = em[a][b] - EA[a] - EB[b];
+                const uint32_t U = (uint32_t)(SA[a] * SB[b]);
+                const int32_t t = (int32_t)shr32(U, sh);
+                Sp[a][b] += t * (GA[a] * GB[b]);
+              }
             }
+          } else {
+            const int4 sb = *reinterpret_cast<const int4 *>(bS + q * kFS + tj);
+            const int4 eb = *reinterpret_cast<const int4 *>(bE + q * kFS + tj);
+            const int4 gb = *reinterpret_cast<const int4 *>(bG + q * kFS + tj);
+            const int32_t SB[4] = {sb.x, sb.y, sb.z, sb.w}, EB[4] = {eb.x, eb.y, eb.z, eb.w}, GB[4] = {gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+            for (int a = 0; a < kFT; a++)
+#pragma unroll
+              for (int b = 0; b < kFT; b++) {
+                const int32_t sh = em[a][b] - EA[a] - EB[b];
+                const uint32_t U = (uint32_t)(SA[a] * SB[b]);
+                const int32_t t = (int32_t)shr32(U, sh);
+                Sp[a][b] += t * (GA[a] * GB[b]);
+              }
+          }
         }
         // ---- the merge with c (lines 5-15)
 #pragma unroll
@@ -556,14 +678,15 @@ template <int ARCH, int ESZ, int SPARSE = 0>
 static int run_fast(const DevModel &m, int kt, int M, int N, int K, const void *A, int64_t lda, const void *Bt,
                     int64_t ldb, const uint32_t *C, int64_t ldc, uint32_t *D, int64_t ldd, cudaStream_t s,
                     const uint8_t *meta = nullptr, int64_t ldm = 0) {
-  const size_t shm = (size_t)6 * fast_chunk(kt) * kFS * 4 + 2 * kFB;
+  const int KC = fast_chunk(kt);
+  const size_t shm = (size_t)(SPARSE == 2 ? 5 * KC : 6 * KC) * kFS * 4 + 2 * kFB;   // gather: 4 (KC / 2) + 3 KC rows
   auto kern = ARCH == MCEMU_ARCH_GA_EARLY ? (m.rne ? gemm_early_kernel<ESZ, SPARSE, 1> : gemm_early_kernel<ESZ, SPARSE, 0>)
                                           : (m.rne ? gemm_late_kernel<ESZ, SPARSE, 1> : gemm_late_kernel<ESZ, SPARSE, 0>);
   if (shm > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm) != cudaSuccess)
     return MCEMU_ERR_UNSUPPORTED;
   dim3 grid((N + kFB - 1) / kFB, (M + kFB - 1) / kFB);
-  const int kblk = SPARSE ? 2 * m.k : m.k;
+  const int kblk = SPARSE == 1 ? 2 * m.k : m.k;     // expansion: a block spans 2 N_FMA dense positions
   kern<<<grid, kFThreads, shm, s>>>(m, kt, kblk, M, N, K, (const uint8_t *)A, lda, meta, ldm, (const uint8_t *)Bt,
                                     ldb, C, ldc, D, ldd);
   if (cudaGetLastError() != cudaSuccess) return MCEMU_ERR_CUDA;

@@ -4,11 +4,12 @@
 
 namespace mcemu {
 
-// 2:4-sparse tile GEMM through the dense fast kernel (expansion while staging);
-// kt and K are the dense instruction and inner sizes.
+// 2:4-sparse tile GEMM through the fast kernels in their gather form: the chain runs
+// over the compressed terms, each reading B at the row its metadata index names; kt
+// and K are the dense instruction and inner sizes.
 bool sparse_fast_ok(const DevModel &m, int kt) {
-  // an even N_FMA keeps every group of four inside one block
-  return gemm_fast_ok(m) && m.k % 2 == 0 && 2 * m.k <= 32 && kt <= 64 && (int)(m.fa.sshift + 1) / 8 <= 2;
+  // any N_FMA: a block of compressed terms may end inside a group of four
+  return gemm_fast_ok(m) && kt <= 64 && (int)(m.fa.sshift + 1) / 8 <= 2;
 }
 
 int launch_sparse24_gemm_fast(const DevModel &m, int kt, int M, int N, int K, const void *Ac, int64_t ldac,
@@ -19,12 +20,12 @@ int launch_sparse24_gemm_fast(const DevModel &m, int kt, int M, int N, int K, co
   if (!sparse_fast_ok(m, kt)) return MCEMU_ERR_UNSUPPORTED;
   if (m.arch == MCEMU_ARCH_GA_EARLY) {
     if (eb == 1)
-      return run_fast<MCEMU_ARCH_GA_EARLY, 1, 1>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
-    return run_fast<MCEMU_ARCH_GA_EARLY, 2, 1>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
+      return run_fast<MCEMU_ARCH_GA_EARLY, 1, 2>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
+    return run_fast<MCEMU_ARCH_GA_EARLY, 2, 2>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
   }
   if (eb == 1)
-    return run_fast<MCEMU_ARCH_GA_LATE, 1, 1>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
-  return run_fast<MCEMU_ARCH_GA_LATE, 2, 1>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
+    return run_fast<MCEMU_ARCH_GA_LATE, 1, 2>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
+  return run_fast<MCEMU_ARCH_GA_LATE, 2, 2>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
 }
 
 }  // namespace mcemu

@@ -305,6 +305,9 @@ SPARSE_CASES = [
     dict(fmt_a="e4m3", fmt_b="e4m3", arch="ga_early", n_fma=8, align_frac=26, out_round="rne"),
     dict(fmt_a="e4m3", fmt_b="e4m3", arch="exact", n_fma=8),
     dict(PRESETS["cdna3_fp8"], fp8_enc="ocp", n_fma=8),
+    # blocks of 5 and 3 compressed terms: blocks that end inside a group of four
+    dict(fmt_a="e4m3", fmt_b="e4m3", arch="ga_early", n_fma=5, align_frac=26, out_round="rne"),
+    dict(PRESETS["cdna3_bf16"], fmt_a="e4m3", fmt_b="e4m3", n_fma=3),
 ]
 
 
@@ -346,17 +349,19 @@ def test_sparse24_gemm_specials_and_bad_metadata(L, fmt, arch):
     assert np.array_equal(D, want), f"{int((D != want).sum())} mismatches"
 
 
-def test_sparse_e4m3_4096_sampled(L):
-    """The 2:4 E4M3 workload at full size: A 4096x4096 compressed to 4096x2048, 16x16x32 tiles."""
+@pytest.mark.parametrize("case", [0, 1])
+def test_sparse_e4m3_4096_sampled(L, case):
+    """The 2:4 E4M3 workload at full size (truncation and RNE outputs): A 4096x4096
+    compressed to 4096x2048, 16x16x32 tiles."""
     M = N = K = 4096
     A, Bt, C = W.gen_sparse_e4m3(M, N, K, seed=4)
     dA = dev(A)
     Ac, meta, viol = L.sparse24_compress("e4m3", dA)
     assert int(viol.item()) == 0
-    spec = SPARSE_CASES[0]
+    spec = SPARSE_CASES[case]
     m = L.Model(spec)
     D = host_u32(L.sparse24_gemm(m, L.tile(1, 16, 16, 32, 8), Ac, meta, dev(Bt), dev(C)))
-    rng = np.random.default_rng(12)
+    rng = np.random.default_rng(12 + case)
     ii = rng.integers(0, M, 128).astype(np.int32)
     jj = rng.integers(0, N, 128).astype(np.int32)
     hAc, hmeta = Ac.cpu().numpy(), meta.cpu().numpy()
