@@ -315,7 +315,7 @@ __device__ __forceinline__ bool f8_exact_fp32(const DevModel &m, const uint32_t 
 // OCP exact-then-round on the FP32 pipe with the undecided sets (ties that the error
 // bound leaves open) batched per warp for the integer path.
 template <int ID, int RM> struct F8GaPairEv {
-  static constexpr bool kSlowQueue = false, kTable = true;
+  static constexpr bool kSpecialQueue = false, kSlowQueue = false, kTable = true;
   static constexpr size_t kTableBytes = sizeof(F8Table);
   static constexpr int kThreads = 512;           // the table lookups want two 512-thread CTAs per SM
   static __device__ __forceinline__ const void *table() { return f8_table<ID>().v; }
@@ -336,7 +336,7 @@ template <int ID, int RM> struct F8GaPairEv {
 };
 
 template <int ID, int RM> struct F8ExactPairEv {
-  static constexpr bool kSlowQueue = true, kTable = false;
+  static constexpr bool kSpecialQueue = false, kSlowQueue = true, kTable = false;
   static constexpr size_t kTableBytes = 0;
   static constexpr int kThreads = kPairThreads;
   static __device__ __forceinline__ const void *table() { return nullptr; }

@@ -236,8 +236,9 @@ __device__ __forceinline__ uint32_t specialxf_classes(const DevModel &m, const u
 // Evaluators of the pair kernel.  eval() returns the result of one set and a flag
 // (bit 0: an Inf/NaN operand or addend, bit 1: the general path decides); special()
 // resolves a flagged set from its words; general() evaluates one set on the integer
-// path.  kSlowQueue: sets with flag 2 are common enough to be batched per warp (else
-// they are evaluated in place).
+// path.  kSpecialQueue: eval() may set flag bit 0 (else it never does, and the kernel
+// keeps no queue for it); kSlowQueue: sets with flag 2 are common enough to be batched
+// per warp (else they are evaluated in place).
 template <int ID> struct PairFmt {
   static constexpr int K = ID == F_XF32T ? 2 : (Fmt<ID>::BYTES == 2 ? 4 : 8);
 };
@@ -256,7 +257,7 @@ __device__ __forceinline__ uint32_t pair_general(const DevModel &m, const uint32
 }
 
 template <int ID, int RM> struct GaPairEv {
-  static constexpr bool kSlowQueue = false, kTable = false;
+  static constexpr bool kSpecialQueue = true, kSlowQueue = false, kTable = false;
   static constexpr size_t kTableBytes = 0;
   static constexpr int kThreads = kPairThreads;
   static __device__ __forceinline__ const void *table() { return nullptr; }
@@ -280,57 +281,64 @@ template <int ID, int RM> struct GaPairEv {
 // XF32 (K = 2) set on the FP32 pipe, every term split against one constant
 // (ExtractScalar of Rump, Ogita and Oishi, "Accurate floating-point summation part I:
 // faithful rounding", SIAM J. Sci. Comput. 31, 2008, Lemma 3.3):
-//  - an element a with exponent field f_a becomes a1 = a 2^(128 - max(f_a, 1)), in
-//    [2, 4) when normal and (0, 2) when subnormal, so p = a1 b1 is exact (8 x 8 or
-//    11 x 11 significand bits) and a b = p 2^(F - 256), F = max(f_a, 1) + max(f_b, 1);
+//  - an element a with exponent field f_a (taken as min(max(f_a, 1), 254)) becomes
+//    a1 = a 2^(128 - f_a), in [2, 4) when normal and (0, 2) when subnormal, so p = a1 b1
+//    is exact (8 x 8 or 11 x 11 significand bits) and a b = p 2^(F - 256), F = f_a + f_b;
 //  - with M = max(F over the products, max(f_c, 1) + 127) every term is scaled by
-//    2^(256 - M): a product to x = p 2^(F - M), |x| < 16, through a scale that is 0 when
-//    F - M < -126 (the product, below 2^-123, is dropped), and c to x_c = c 2^(256 - M),
+//    2^(256 - M): a product to x = p 2^(F - M), |x| < 16, and c to x_c = c 2^(256 - M),
 //    |x_c| < 8, by two exact power-of-two multiplies (exponents in [-126, 64]; only a
-//    subnormal x_c, below 2^-126, is rounded);
+//    subnormal x_c, below 2^-126, is rounded).  A product with F - M < -126 keeps the
+//    scale 2^-126 instead: the term it adds and the one it stands for are both below
+//    2^-122;
 //  - with sigma = 2^7 (K = 4) or 2^6 (K = 2), q = fl(sigma + x) - sigma and r = x - q are
 //    exact (x enters through one fused multiply-add each); every q is a multiple of
 //    ulp(sigma) / 2 and |sum q| < sigma, so tau = sum q is exact, and |r| <= ulp(sigma) / 2;
 //  - P = fl(sum r) (K additions) is off from sum r by at most gamma_K (K + 1) ulp(sigma)
 //    / 2 < 2^-36.6 (K = 4) or 2^-39.4 (K = 2) (Higham, Accuracy and Stability of Numerical
-//    Algorithms, Sec. 4.2); with the dropped terms that stays below kBound;
+//    Algorithms, Sec. 4.2); with the rescaled small terms that stays below kBound;
 //  - when |tau| >= |P|, Dekker's Fast2Sum gives t + r = tau + P exactly, so the exact sum
 //    is t + r + d with |d| < kBound, and t is its RNE rounding when |r| + kBound is below
 //    half the spacing of the floats next to t (the smaller one, below |t|).
 // The rounded t goes back by 2^(M - 256) on its exponent field; one at or beyond 2^128
 // is +-Inf.  A zero, tiny (< 2^-124 after scaling), subnormal or undecided result
-// returns 2 (the integer path).  sw is nonzero when an operand or c is Inf or NaN; the
-// result is then meaningless and the caller resolves the set from its classes.
+// returns 2 (the integer path).  Special values:
+//  - BF16: an Inf or NaN operand or c keeps its class through the positive scales, so
+//    tau is the IEEE sum's special value: NaN (nan_bits) for a NaN, Inf * 0 or Inf - Inf,
+//    else the signed Inf (the model's special results); sw stays 0;
+//  - XF32: a NaN whose mantissa lies in the 13 truncated bits would read as an Inf
+//    here, so sw flags any operand or c with an exponent field of all ones and the
+//    caller resolves the set from its raw words.
 template <int ID>
 __device__ __forceinline__ int sigma_exact_rn(const uint32_t (&wa)[2], const uint32_t (&wb)[2], uint32_t cb,
-                                              uint32_t &out, uint32_t &sw) {
+                                              uint32_t nan_bits, uint32_t &out, uint32_t &sw) {
   static_assert(ID == F_BF16 || ID == F_XF32T, "BF16 or truncated XF32 elements");
   constexpr int K = ID == F_BF16 ? 4 : 2;
   constexpr float kSigma = K == 4 ? 0x1p7f : 0x1p6f;
   constexpr float kBound = K == 4 ? 0x1p-36f : 0x1p-39f;
   constexpr uint32_t kE255 = 255u << 23, kE127 = 127u << 23;
   float p[K];
-  uint32_t F23[K];                                     // F << 23 (F <= 510: fits unsigned)
-  uint32_t top = 0;                                    // the largest exponent field(s) of a and b
+  uint32_t F23[K];                                     // F << 23 (F <= 508: fits unsigned)
   if constexpr (ID == F_BF16) {
 #pragma unroll
     for (int i = 0; i < 2; i++) {
-      // max(field, 1) << 7 in each 16-bit half; << 16 and the high half's mask put it at 23
-      const uint32_t Ea = vmax2(wa[i] & 0x7F807F80u, 0x00800080u);
-      const uint32_t Eb = vmax2(wb[i] & 0x7F807F80u, 0x00800080u);
-      top = vmax2(top, vmax2(Ea, Eb));
+      // min(max(field, 1), 254) << 7 in each 16-bit half; << 16 and the high half's mask
+      // put it at bit 23
+      const uint32_t Ea = vmin2(vmax2(wa[i] & 0x7F807F80u, 0x00800080u), 0x7F007F00u);
+      const uint32_t Eb = vmin2(vmax2(wb[i] & 0x7F807F80u, 0x00800080u), 0x7F007F00u);
       const float a_lo = __fmul_rn(__uint_as_float(wa[i] << 16), __uint_as_float(kE255 - (Ea << 16)));
       const float b_lo = __fmul_rn(__uint_as_float(wb[i] << 16), __uint_as_float(kE255 - (Eb << 16)));
       const float a_hi = __fmul_rn(__uint_as_float(wa[i] & 0xFFFF0000u), __uint_as_float(kE255 - (Ea & 0xFFFF0000u)));
       const float b_hi = __fmul_rn(__uint_as_float(wb[i] & 0xFFFF0000u), __uint_as_float(kE255 - (Eb & 0xFFFF0000u)));
       p[2 * i] = __fmul_rn(a_lo, b_lo);
       p[2 * i + 1] = __fmul_rn(a_hi, b_hi);
-      const uint32_t Es = Ea + Eb;                     // per half (F << 7) <= 510 << 7: no carry
+      const uint32_t Es = Ea + Eb;                     // per half (F << 7) <= 508 << 7: no carry
       F23[2 * i] = Es << 16;
       F23[2 * i + 1] = Es & 0xFFFF0000u;
     }
-    top = (top + 0x00800080u) & 0x80008000u;           // a field of all ones in either half
+    sw = 0u;
   } else {
+    // the fields are not clamped: a set with an Inf or NaN is resolved by the caller
+    uint32_t top = cb & 0x7F800000u;
 #pragma unroll
     for (int l = 0; l < 2; l++) {
       const uint32_t xa = wa[l] & 0xFFFFE000u, xb = wb[l] & 0xFFFFE000u;   // 10 mantissa bits
@@ -340,11 +348,10 @@ __device__ __forceinline__ int sigma_exact_rn(const uint32_t (&wa)[2], const uin
                        __fmul_rn(__uint_as_float(xb), __uint_as_float(kE255 - Eb)));
       F23[l] = Ea + Eb;
     }
-    top = top == kE255 ? 1u : 0u;
+    sw = top == kE255 ? 1u : 0u;
   }
   const uint32_t cf = cb & 0x7F800000u;
-  sw = top | (cf == kE255 ? 1u : 0u);
-  uint32_t M23 = max(cf, 1u << 23) + kE127;
+  uint32_t M23 = (ID == F_BF16 ? min(max(cf, 1u << 23), 254u << 23) : max(cf, 1u << 23)) + kE127;
 #pragma unroll
   for (int l = 0; l < K; l++) M23 = max(M23, F23[l]);
   // c * 2^k, k = 256 - M in [-252, 128], as 2^k1 2^k2 with k1 = floor(k / 2)
@@ -356,10 +363,14 @@ __device__ __forceinline__ int sigma_exact_rn(const uint32_t (&wa)[2], const uin
   float P = __fadd_rn(xc, -tq);
 #pragma unroll
   for (int l = 0; l < K; l++) {
-    const float sc = __uint_as_float(kE127 - min(M23 - F23[l], kE127));   // 2^(F - M), 0 below 2^-126
+    const float sc = __uint_as_float(kE127 - min(M23 - F23[l], 126u << 23));   // 2^(F - M), >= 2^-126
     const float q = __fadd_rn(__fmaf_rn(p[l], sc, kSigma), -kSigma);
     tq = __fadd_rn(tq, q);
     P = __fadd_rn(P, __fmaf_rn(p[l], sc, -q));
+  }
+  if (!(fabsf(tq) <= 0x1p7f)) {                        // an Inf or NaN operand or c
+    out = tq != tq ? nan_bits : __float_as_uint(tq);
+    return 0;
   }
   const float t = __fadd_rn(tq, P);
   const float r = __fadd_rn(P, -__fadd_rn(t, -tq));
@@ -373,14 +384,15 @@ __device__ __forceinline__ int sigma_exact_rn(const uint32_t (&wa)[2], const uin
   return ok ? 0 : 2;
 }
 
-// Exact-then-round on the FP32 pipe: FP16 with exact fp32 products (special values
-// from the IEEE sum, in line); BF16 and truncated XF32 with RNE through sigma_exact_rn,
-// with RZ through exact_scaled, whose error bound follows the terms (an RZ decision
-// needs the sign of a remainder that can lie far below any fixed bound); special values
-// of those two queued and resolved from their classes.  A rounding the error bound leaves
+// Exact-then-round on the FP32 pipe: FP16 with exact fp32 products and BF16 with RNE
+// through sigma_exact_rn, both with special values from the IEEE sums in line;
+// truncated XF32 with RNE through sigma_exact_rn, and BF16 and XF32 with RZ through
+// exact_scaled, whose error bound follows the terms (an RZ decision needs the sign of a
+// remainder that can lie far below any fixed bound), with special values queued and
+// resolved from their classes.  A rounding the error bound leaves
 // undecided, a subnormal addend or result goes to the integer path, 32 at a time.
 template <int ID, int RM> struct ExactPairEv {
-  static constexpr bool kSlowQueue = true, kTable = false;
+  static constexpr bool kSpecialQueue = ID == F_XF32T || (ID == F_BF16 && RM == 0), kSlowQueue = true, kTable = false;
   static constexpr size_t kTableBytes = 0;
   static constexpr int kThreads = kPairThreads;
   static __device__ __forceinline__ const void *table() { return nullptr; }
@@ -399,7 +411,7 @@ template <int ID, int RM> struct ExactPairEv {
       flag = exact_fp32_sum<4>(p, cb, RM, m.nan_bits, r) ? 2u : 0u;
     } else if constexpr (RM == 1) {
       uint32_t sw;
-      const int st = sigma_exact_rn<ID>(wa, wb, cb, r, sw);
+      const int st = sigma_exact_rn<ID>(wa, wb, cb, m.nan_bits, r, sw);
       flag = sw ? 1u : (st ? 2u : 0u);
     } else {
       uint32_t sw = (cb & 0x7F800000u) == 0x7F800000u;
@@ -486,14 +498,15 @@ __global__ void __launch_bounds__(Ev::kThreads) pair_kernel(const __grid_constan
     __syncthreads();
     tab = reinterpret_cast<const uint16_t *>(pair_table);
   }
+  constexpr int kSpecWarps = Ev::kSpecialQueue ? Ev::kThreads / 32 : 1;
   constexpr int kSlowWarps = Ev::kSlowQueue ? Ev::kThreads / 32 : 1;
-  __shared__ uint4 queue_ab[Ev::kThreads / 32][kPairQueue];
-  __shared__ uint2 queue_ci[Ev::kThreads / 32][kPairQueue];
+  __shared__ uint4 queue_ab[kSpecWarps][kPairQueue];
+  __shared__ uint2 queue_ci[kSpecWarps][kPairQueue];
   __shared__ uint4 slow_ab[kSlowWarps][kPairQueue];
   __shared__ uint2 slow_ci[kSlowWarps][kPairQueue];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t below = (1u << lane) - 1u;
-  const PairQueue q{queue_ab[warp], queue_ci[warp]};
+  const PairQueue q{queue_ab[Ev::kSpecialQueue ? warp : 0], queue_ci[Ev::kSpecialQueue ? warp : 0]};
   const PairQueue qs{slow_ab[Ev::kSlowQueue ? warp : 0], slow_ci[Ev::kSlowQueue ? warp : 0]};
   int qn = 0, qsn = 0;                                          // warp-uniform
   const uint32_t stride = gridDim.x * blockDim.x;
@@ -531,11 +544,12 @@ __global__ void __launch_bounds__(Ev::kThreads) pair_kernel(const __grid_constan
       }
       __stcs(d + p, r);
     }
-    pair_enqueue(q, qn, (f0 & 1u) != 0u, (f1 & 1u) != 0u, xa, xb, xc, p, below, lane, d32, special);
+    if constexpr (Ev::kSpecialQueue)
+      pair_enqueue(q, qn, (f0 & 1u) != 0u, (f1 & 1u) != 0u, xa, xb, xc, p, below, lane, d32, special);
     if constexpr (Ev::kSlowQueue)
       pair_enqueue(qs, qsn, f0 == 2u, f1 == 2u, xa, xb, xc, p, below, lane, d32, general);
   }
-  pair_drain(q, qn, lane, d32, special);
+  if constexpr (Ev::kSpecialQueue) pair_drain(q, qn, lane, d32, special);
   if constexpr (Ev::kSlowQueue) pair_drain(qs, qsn, lane, d32, general);
 }
 

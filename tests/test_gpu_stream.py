@@ -350,6 +350,53 @@ def _scale_extremes(fmt, n, k, seed):
     return a, b, c
 
 
+def _special_mix(fmt, n, k, seed):
+    """Elements drawn from +-Inf, NaN, +-0, the largest and smallest binades and
+    random bits (an Inf next to a tiny element while other products are huge, Inf * 0,
+    Inf - Inf, NaN among huge terms), c likewise."""
+    rng = np.random.default_rng(seed)
+    mb = {"bf16": 7, "fp16": 10, "xf32": 23}[fmt]
+    eb = 5 if fmt == "fp16" else 8
+    dt = np.uint32 if fmt == "xf32" else np.uint16
+    emax = (1 << eb) - 1
+
+    def draw(shape, mbits, ebits):
+        kind = rng.integers(0, 8, shape)
+        field = rng.integers(0, 1 << ebits, shape)
+        field = np.where(kind == 0, (1 << ebits) - 1, field)                       # Inf / NaN
+        field = np.where(kind == 1, 0, field)                                       # zero / tiny
+        field = np.where(kind == 2, rng.integers((1 << ebits) - 6, (1 << ebits) - 1, shape), field)  # huge
+        field = np.where(kind == 3, rng.integers(0, 4, shape), field)               # tiny
+        mant = rng.integers(0, 1 << mbits, shape)
+        mant = np.where((kind == 0) & (rng.random(shape) < 0.6), 0, mant)           # Inf more often than NaN
+        mant = np.where((kind == 1) & (rng.random(shape) < 0.7), 0, mant)           # +-0
+        sign = rng.integers(0, 2, shape)
+        return (sign << (mbits + ebits)) | (field << mbits) | mant
+
+    a = draw((n, k), mb, eb).astype(dt)
+    b = draw((n, k), mb, eb).astype(dt)
+    if fmt == "xf32":
+        a &= dt(0xFFFFE000)
+        b &= dt(0xFFFFE000)
+    c = draw(n, 23, 8).astype(np.uint32)
+    assert emax > 0
+    return a, b, c
+
+
+@pytest.mark.parametrize("fmt,k", [("bf16", 4), ("xf32", 2), ("fp16", 4)])
+def test_special_operand_mixes(L, fmt, k):
+    """Every stream model on sets dense in Inf, NaN, zeros and extreme binades: the
+    special result (NaN for a NaN, Inf * 0 or Inf - Inf, else the signed Inf) and the
+    finite results around them."""
+    a, b, c = _special_mix(fmt, 50000, k, seed=97)
+    for name, spec in block_models(fmt, k).items():
+        for out_round in ("rne", "rtz") if name == "ieee_exact" else (None,):
+            s = spec if out_round is None else dict(spec, out_round=out_round)
+            got = gpu_block(L, s, a, b, c)
+            want = oracle.block_fma_parallel(s, a, b, c, threads=8)
+            assert np.array_equal(got, want), f"{fmt} {name} {out_round}\n" + mismatches(got, want, a, b, c)
+
+
 @pytest.mark.parametrize("fmt,k", [("bf16", 4), ("xf32", 2)])
 def test_exact_scale_extremes(L, fmt, k):
     """Exact-then-round, RNE and RTZ, on BF16/XF32 sets at the ends of the exponent range,
