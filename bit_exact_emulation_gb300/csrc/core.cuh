@@ -1303,10 +1303,15 @@ __device__ __forceinline__ int exact_scaled(const uint32_t (&wa)[NW], const uint
     eref = max(eref, el[l]);
   }
   float bx = 0.0f;                                          // bound of the dropped terms
+  uint32_t dsg = 0u;                                        // their signs: bit 0 +, bit 1 -
   float sv = 0.0f;
   if (cf) {
-    if ((int32_t)cf - eref >= 1) sv = __uint_as_float(cb - ((uint32_t)eref << 23));
-    else bx = 0x1p-125f;
+    if ((int32_t)cf - eref >= 1) {
+      sv = __uint_as_float(cb - ((uint32_t)eref << 23));
+    } else {
+      bx = 0x1p-125f;
+      dsg = (cb >> 31) + 1u;
+    }
   }
   float e[K];
 #pragma unroll
@@ -1314,19 +1319,57 @@ __device__ __forceinline__ int exact_scaled(const uint32_t (&wa)[NW], const uint
     const int32_t d = el[l] - 2 - eref;
     const bool keep = d >= DMIN;
     const float sc = __uint_as_float(keep ? (uint32_t)(d + 127) << 23 : 0u);
-    if (!keep) bx = __fadd_ru(bx, kDrop);
+    if (!keep) {
+      bx = __fadd_ru(bx, kDrop);
+      if (pp[l] != 0.0f) dsg |= (__float_as_uint(pp[l]) >> 31) + 1u;
+    }
     two_sum(sv, __fmul_rn(pp[l], sc), sv, e[l]);
   }
-  float E = e[0], a = fabsf(e[0]);
-#pragma unroll
-  for (int l = 1; l < K; l++) {
-    E = __fadd_rn(E, e[l]);
-    a = __fadd_ru(a, fabsf(e[l]));
-  }
-  constexpr float kGamma = K <= 2 ? 0x1p-23f : K <= 3 ? 0x1p-22f : K <= 5 ? 0x1p-21f : K <= 9 ? 0x1p-20f
-                                                     : K <= 17 ? 0x1p-19f : 0x1p-18f;
   uint32_t tb;
-  if (exact_fp32_round(sv, E, __fadd_ru(__fmul_ru(a, kGamma), bx), rne, tb)) return 2;
+  if (rne) {
+    float E = e[0], a = fabsf(e[0]);
+#pragma unroll
+    for (int l = 1; l < K; l++) {
+      E = __fadd_rn(E, e[l]);
+      a = __fadd_ru(a, fabsf(e[l]));
+    }
+    constexpr float kGamma = K <= 2 ? 0x1p-23f : K <= 3 ? 0x1p-22f : K <= 5 ? 0x1p-21f : K <= 9 ? 0x1p-20f
+                                                       : K <= 17 ? 0x1p-19f : 0x1p-18f;
+    if (exact_fp32_round(sv, E, __fadd_ru(__fmul_ru(a, kGamma), bx), 1, tb)) return 2;
+  } else {
+    // RZ needs the sign of S - t, which can lie far below any error bound: the errors
+    // are summed by TwoSum as well (E + sum f = sum e exactly, fb >= sum |f|, 0 when
+    // that sum is exact), so S = t + r + (sum f) + (dropped terms), and the sign of the
+    // remainder is known when |r| clears the rest, or when the rest is one-signed
+    // dropped terms (fb = 0) agreeing with r or standing alone (r = 0)
+    float E = e[0], fb = 0.0f;
+#pragma unroll
+    for (int l = 1; l < K; l++) {
+      float f;
+      two_sum(E, e[l], E, f);
+      fb = __fadd_ru(fb, fabsf(f));
+    }
+    float t, r;
+    two_sum(sv, E, t, r);
+    tb = __float_as_uint(t);
+    const uint32_t ef = tb & 0x7F800000u;
+    if (ef < (3u << 23) || ef == 0x7F800000u) return 2;    // |t| < 2^-124, or beyond
+    const float b = __fadd_ru(fb, bx);
+    if (b >= __fmul_rn(__uint_as_float(ef), 0x1p-25f)) return 2;
+    const float sr = (tb >> 31) ? -r : r;                   // r measured away from zero
+    int dir;                                                // sign of S - t, away from zero
+    if (sr >= b) dir = 1;                                   // S = t or beyond it: RZ gives t
+    else if (-sr > b) dir = -1;
+    else if (fb == 0.0f && (dsg == 1u || dsg == 2u) && ef >= (56u << 23) &&
+             (r == 0.0f || (__float_as_uint(r) >> 31) + 1u == dsg)) {
+      // the dropped terms, below 2^-98 in all and under ulp(t) / 2 for |t| >= 2^-71,
+      // decide alone (r = 0) or agree with r
+      dir = ((tb >> 31) + 1u == dsg) ? 1 : -1;
+    } else {
+      return 2;
+    }
+    if (dir < 0) tb -= 1u;                                   // the neighbour of t toward zero
+  }
   const int32_t fr = (int32_t)((tb >> 23) & 0xFFu) + eref;
   if (fr > 254) {                                           // the rounded sum reaches 2^128
     out = (tb & 0x80000000u) | (rne ? 0x7F800000u : 0x7F7FFFFFu);
