@@ -53,30 +53,18 @@ __device__ __forceinline__ uint32_t stage_elem(const FmtDev &f, uint32_t x, int3
 // Stage one K-chunk of the CTA's A rows and B columns into shared memory, decoded:
 // element (r, q) of the chunk goes to [q][r] as significand, exponent (kZeroE for a
 // zero) and sign +-1; B significands are shifted left by bshift.  A row or column
-// that holds an Inf/NaN (or, for SPARSE, invalid metadata) is flagged.
-template <int ESZ, int SPARSE>
+// that holds an Inf/NaN is flagged.
+template <int ESZ>
 __device__ __forceinline__ void stage_chunk(const DevModel &m, int bshift, int i0, int j0, int k0, int kc, int KC,
                                             int M, int N, const uint8_t *__restrict__ A, int64_t lda,
-                                            const uint8_t *__restrict__ meta, int64_t ldm,
                                             const uint8_t *__restrict__ Bt, int64_t ldb, int32_t *aS, int32_t *aE,
                                             int32_t *aG, int32_t *bS, int32_t *bE, int32_t *bG, uint8_t *aSpec,
                                             uint8_t *bSpec) {
   for (int e = threadIdx.x; e < kFB * KC; e += blockDim.x) {
     const int r = e / KC, q = e % KC;
     int32_t S = 0, E = kZeroE, G = 1;
-    if constexpr (SPARSE) {
-      if (i0 + r < M && q < kc) {
-        const int kd = k0 + q, g = kd >> 2, p = kd & 3;
-        const uint32_t mb = meta[(int64_t)(i0 + r) * ldm + g];
-        const uint32_t idx0 = mb & 3u, idx1 = (mb >> 2) & 3u;
-        if (idx0 >= idx1) aSpec[r] = 1;                  // not a valid 2:4 pattern
-        const int t = (p == (int)idx0) ? 0 : (p == (int)idx1) ? 1 : -1;
-        if (t >= 0 && stage_elem(m.fa, fld<ESZ>(A, (int64_t)(i0 + r) * lda + 2 * g + t), S, E, G)) aSpec[r] = 1;
-      }
-    } else {
-      if (i0 + r < M && q < kc && stage_elem(m.fa, fld<ESZ>(A, (int64_t)(i0 + r) * lda + k0 + q), S, E, G))
-        aSpec[r] = 1;
-    }
+    if (i0 + r < M && q < kc && stage_elem(m.fa, fld<ESZ>(A, (int64_t)(i0 + r) * lda + k0 + q), S, E, G))
+      aSpec[r] = 1;
     aS[q * kFS + r] = S; aE[q * kFS + r] = E; aG[q * kFS + r] = G;
     S = 0; E = kZeroE; G = 1;
     if (j0 + r < N && q < kc && stage_elem(m.fb, fld<ESZ>(Bt, (int64_t)(j0 + r) * ldb + k0 + q), S, E, G))
@@ -85,7 +73,7 @@ __device__ __forceinline__ void stage_chunk(const DevModel &m, int bshift, int i
   }
 }
 
-// The gather form of the 2:4-sparse GEMM (SPARSE = 2): a chunk holds KCA compressed
+// The gather form of the 2:4-sparse GEMM (SPARSE = 1): a chunk holds KCA compressed
 // terms of A (compressed k0c .. k0c + kcc) and the 2 KCA dense rows of B^T they draw on.
 // Compressed term q of row r goes to [q][r] as (S, E, sign) plus, in aI, the offset of
 // its B row in the panel, (4 (q / 2) + idx) * kFS with idx the metadata index of its
@@ -178,14 +166,11 @@ __host__ __device__ __forceinline__ uint32_t redo_mark(const DevModel &m) {
 
 // Both kernels below: C == nullptr stands for C = 0.
 //
-// SPARSE = 1: A is given 2:4-compressed (Ac [M][K/2], meta [M][K/4]) and is expanded
-// into the dense panel while staging; kt and K are then dense sizes and a block spans
-// kblk = 2 N_FMA dense positions.  A block of N_FMA compressed terms covers exactly
-// those positions (groups of four never straddle blocks), and the positions the
-// expansion fills with zeros add zero products, which take no part in e_max and add
-// nothing to the aligned sum: the result is the compressed chain's.  The cases where
-// that argument needs finite operands, a nonzero sum or valid metadata (idx0 < idx1)
-// are the ones sent to the general evaluator of the compressed chain.
+// SPARSE = 1: A is given 2:4-compressed (Ac [M][K/2], meta [M][K/4]); kt and K are
+// dense sizes.  The chain runs over the compressed terms (kt / 2 per instruction,
+// blocks of N_FMA terms), and each term reads the B row its metadata index names
+// (stage_chunk_gather).  Rows with invalid metadata (idx0 >= idx1) and rows or
+// columns with an Inf/NaN go to the general evaluator of the compressed chain.
 //
 // Early-c global alignment (Table 3's early-c model) with the accumulator carried
 // between blocks as f * 2^g: f is the block result's rounded significand as an
@@ -213,7 +198,7 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_early_kernel(const __grid_c
                                                                 int64_t ldb, const uint32_t *C, int64_t ldc,
                                                                 uint32_t *D, int64_t ldd) {
   extern __shared__ int32_t fsm[];
-  constexpr bool GATHER = SPARSE == 2;
+  constexpr bool GATHER = SPARSE != 0;
   const int KC = fast_chunk(kt);                                         // dense positions per chunk
   const int KCA = GATHER ? KC / 2 : KC;                                  // A panel rows
   int32_t *aS = fsm, *aE = aS + KCA * kFS, *aG = aE + KCA * kFS;        // [KCA][kFS]
@@ -261,8 +246,7 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_early_kernel(const __grid_c
       stage_chunk_gather<ESZ>(m, m.P0, i0, j0, k0 / 2, kc / 2, KCA, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, aI,
                               bS, bE, bG, aSpec, bSpec);
     else
-      stage_chunk<ESZ, SPARSE>(m, m.P0, i0, j0, k0, kc, KC, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, bS, bE, bG,
-                               aSpec, bSpec);
+      stage_chunk<ESZ>(m, m.P0, i0, j0, k0, kc, KC, M, N, A, lda, Bt, ldb, aS, aE, aG, bS, bE, bG, aSpec, bSpec);
     __syncthreads();
     // an Inf/NaN in a row of A or a column of B (or invalid metadata) sends the whole
     // row / column of this thread's tile to the fixup pass
@@ -447,7 +431,7 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_late_kernel(const __grid_co
                                                                int64_t ldb, const uint32_t *C, int64_t ldc,
                                                                uint32_t *D, int64_t ldd) {
   extern __shared__ int32_t fsm[];
-  constexpr bool GATHER = SPARSE == 2;
+  constexpr bool GATHER = SPARSE != 0;
   const int KC = fast_chunk(kt);                                         // dense positions per chunk
   const int KCA = GATHER ? KC / 2 : KC;                                  // A panel rows
   int32_t *aS = fsm, *aE = aS + KCA * kFS, *aG = aE + KCA * kFS;        // [KCA][kFS]
@@ -492,8 +476,7 @@ __global__ void __launch_bounds__(kFThreads, 2) gemm_late_kernel(const __grid_co
       stage_chunk_gather<ESZ>(m, m.P0, i0, j0, k0 / 2, kc / 2, KCA, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, aI,
                               bS, bE, bG, aSpec, bSpec);
     else
-      stage_chunk<ESZ, SPARSE>(m, m.P0, i0, j0, k0, kc, KC, M, N, A, lda, meta, ldm, Bt, ldb, aS, aE, aG, bS, bE, bG,
-                               aSpec, bSpec);
+      stage_chunk<ESZ>(m, m.P0, i0, j0, k0, kc, KC, M, N, A, lda, Bt, ldb, aS, aE, aG, bS, bE, bG, aSpec, bSpec);
     __syncthreads();
 #pragma unroll
     for (int a = 0; a < kFT; a++)
@@ -679,14 +662,14 @@ static int run_fast(const DevModel &m, int kt, int M, int N, int K, const void *
                     int64_t ldb, const uint32_t *C, int64_t ldc, uint32_t *D, int64_t ldd, cudaStream_t s,
                     const uint8_t *meta = nullptr, int64_t ldm = 0) {
   const int KC = fast_chunk(kt);
-  const size_t shm = (size_t)(SPARSE == 2 ? 5 * KC : 6 * KC) * kFS * 4 + 2 * kFB;   // gather: 4 (KC / 2) + 3 KC rows
+  const size_t shm = (size_t)(SPARSE ? 5 * KC : 6 * KC) * kFS * 4 + 2 * kFB;   // gather: 4 (KC / 2) + 3 KC rows
   auto kern = ARCH == MCEMU_ARCH_GA_EARLY ? (m.rne ? gemm_early_kernel<ESZ, SPARSE, 1> : gemm_early_kernel<ESZ, SPARSE, 0>)
                                           : (m.rne ? gemm_late_kernel<ESZ, SPARSE, 1> : gemm_late_kernel<ESZ, SPARSE, 0>);
   if (shm > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm) != cudaSuccess)
     return MCEMU_ERR_UNSUPPORTED;
   dim3 grid((N + kFB - 1) / kFB, (M + kFB - 1) / kFB);
-  const int kblk = SPARSE == 1 ? 2 * m.k : m.k;     // expansion: a block spans 2 N_FMA dense positions
+  const int kblk = m.k;                             // a block of N_FMA (compressed) terms
   kern<<<grid, kFThreads, shm, s>>>(m, kt, kblk, M, N, K, (const uint8_t *)A, lda, meta, ldm, (const uint8_t *)Bt,
                                     ldb, C, ldc, D, ldd);
   if (cudaGetLastError() != cudaSuccess) return MCEMU_ERR_CUDA;

@@ -20,12 +20,12 @@ int launch_sparse24_gemm_fast(const DevModel &m, int kt, int M, int N, int K, co
   if (!sparse_fast_ok(m, kt)) return MCEMU_ERR_UNSUPPORTED;
   if (m.arch == MCEMU_ARCH_GA_EARLY) {
     if (eb == 1)
-      return run_fast<MCEMU_ARCH_GA_EARLY, 1, 2>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
-    return run_fast<MCEMU_ARCH_GA_EARLY, 2, 2>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
+      return run_fast<MCEMU_ARCH_GA_EARLY, 1, 1>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
+    return run_fast<MCEMU_ARCH_GA_EARLY, 2, 1>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
   }
   if (eb == 1)
-    return run_fast<MCEMU_ARCH_GA_LATE, 1, 2>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
-  return run_fast<MCEMU_ARCH_GA_LATE, 2, 2>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
+    return run_fast<MCEMU_ARCH_GA_LATE, 1, 1>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
+  return run_fast<MCEMU_ARCH_GA_LATE, 2, 1>(m, kt, M, N, K, Ac, ldac, Bt, ldb, C, ldc, D, ldd, s, meta, ldm);
 }
 
 }  // namespace mcemu
