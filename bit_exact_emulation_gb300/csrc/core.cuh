@@ -1266,14 +1266,18 @@ __device__ __forceinline__ int exact_fp32_round(float s, float E, float b, int r
 //    product further down is dropped, and 2^(DMIN + 4) > |p' 2^d| joins the bound;
 //  - c * 2^-e_ref (|.| < 2) is c with its exponent field lowered by e_ref while that
 //    stays normal, else dropped with 2^-125 in the bound;
-// then the sum, its bound and the rounding decision are exact_fp32_sum's (K + 1 terms).
+// then the TwoSum cascade of exact_fp32_sum adds the K + 1 terms.  With RNE its error
+// bound and decision follow exact_fp32_sum.  With RZ the errors are summed by TwoSum too
+// (the bound is 0 when that sum is exact), and a kept sum that is exact takes its
+// direction from the dropped terms when they all have one sign (RZ needs the sign of
+// the remainder, which no fixed bound gives).
 // The scaled result t' goes back by adding e_ref to its exponent field.  When that
 // reaches 2^128 the correctly rounded sum overflows: +-Inf under RNE, +-max-finite
 // under RTZ.  A subnormal result, a subnormal c and an undecided rounding return 2
 // (the integer path).  Inf/NaN operands and the CDNA 3 product-overflow rule are the
-// caller's.  e_ref may exceed the largest
-// nonzero product's exponent (a zero operand counts with E = -126): that only moves
-// terms toward the dropped range, and the bound covers them.
+// caller's.  e_ref may exceed the largest nonzero product's exponent (a zero operand
+// counts with E = -126): that only moves terms toward the dropped range, and the bound
+// covers them.
 template <int ID, int K, int NW>
 __device__ __forceinline__ int exact_scaled(const uint32_t (&wa)[NW], const uint32_t (&wb)[NW], uint32_t cb,
                                             int rne, uint32_t &out) {
