@@ -15,6 +15,7 @@ sets (weak scaling, no collective on the data path).
 """
 import argparse
 import hashlib
+import re
 import json
 import os
 import subprocess
@@ -177,15 +178,22 @@ def run_reference(args, rank):
 STREAM_SOURCES = ("core.cuh", "model.h", "stream.cu", "stream_fp8.cu", "stream_pair.cuh")
 
 
+def _code_only(text):
+    """C/C++ source without its comments and with whitespace runs collapsed: what the
+    compiler sees, so that a comment edit leaves the hash unchanged."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash():
-    """Hash of the sources the block-FMA stream kernels are compiled from."""
+    """Hash of the code (comments stripped) the block-FMA stream kernels are compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_exact_emulation_gb300", "csrc")
-    for name in STREAM_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
-    with open(os.path.join(ROOT, "include", "mcemu.h"), "rb") as f:
-        h.update(f.read())
+    paths = [os.path.join(csrc, name) for name in STREAM_SOURCES] + [os.path.join(ROOT, "include", "mcemu.h")]
+    for path in paths:
+        with open(path, encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
