@@ -1256,6 +1256,67 @@ __device__ __forceinline__ int exact_fp32_round(float s, float E, float b, int r
   return 2;
 }
 
+// The sign of r + (the terms exact_scaled drops): -1, +1, or 0 when it is not decided.
+// The dropped terms are products with E_a + E_b - 2 - e_ref < DMIN, and c (exponent
+// e_c) when cdrop.  They are summed by the same rescaling one level down: e2 = the
+// largest dropped exponent, every dropped term scaled by 2^-e2 (exact while within DMIN
+// of it, else bounded), summed in fp32 with the upward-rounded bound gamma_K sum |x|
+// plus the bounded ones, so their sum D lies in [lo, hi] * 2^(e2 - e_ref) in magnitude.
+// r (on the 2^e_ref scale) decides when it has D's sign, or when its binade is clear of
+// [lo, hi]'s scaled binades; D decides alone when r = 0 and lo > 0.
+template <int ID, int K>
+__device__ __forceinline__ int dropped_sum_sign(const float (&pp)[K], const int32_t (&el)[K], int32_t eref,
+                                                uint32_t cb, int32_t ce, bool cdrop, float r) {
+  constexpr int32_t DMIN = ID == F_BF16 ? -110 : -104;
+  constexpr float kDrop = ID == F_BF16 ? 0x1p-106f : 0x1p-100f;
+  int32_t e2 = cdrop ? ce + 2 : -100000;                    // c's value is below 2^(e_c + 1)
+#pragma unroll
+  for (int l = 0; l < K; l++)
+    if (el[l] - 2 - eref < DMIN && pp[l] != 0.0f) e2 = max(e2, el[l]);
+  float sum = 0.0f, mag = 0.0f, bnd = 0.0f;
+#pragma unroll
+  for (int l = 0; l < K; l++) {
+    if (!(el[l] - 2 - eref < DMIN) || pp[l] == 0.0f) continue;
+    const int32_t d = el[l] - 2 - e2;                         // <= -2
+    if (d < DMIN) {
+      bnd = __fadd_ru(bnd, kDrop);
+      continue;
+    }
+    const float x = __fmul_rn(pp[l], __uint_as_float((uint32_t)(d + 127) << 23));
+    sum = __fadd_rn(sum, x);
+    mag = __fadd_ru(mag, fabsf(x));
+  }
+  if (cdrop) {
+    if (ce - e2 >= -126) {                                    // c * 2^-e2 is normal: exact
+      // a normal c by its exponent field; a subnormal one (e_c = -126, so e2 <= 0) by a
+      // multiply with 2^-e2 <= 2^124
+      const float x = (cb & 0x7F800000u) ? __uint_as_float(cb - ((uint32_t)e2 << 23))
+                                         : __fmul_rn(__uint_as_float(cb), __uint_as_float((uint32_t)(127 - e2) << 23));
+      sum = __fadd_rn(sum, x);
+      mag = __fadd_ru(mag, fabsf(x));
+    } else {
+      bnd = __fadd_ru(bnd, 0x1p-125f);
+    }
+  }
+  // K + 1 terms at most: K additions, gamma_K < (K + 1) 2^-24
+  bnd = __fadd_ru(bnd, __fmul_ru(mag, (float)(K + 1) * 0x1p-24f));
+  const float hi = __fadd_ru(fabsf(sum), bnd), lo = __fadd_rd(fabsf(sum), -bnd);
+  const int sd = lo > 0.0f ? (sum < 0.0f ? -1 : 1) : 0;
+  if (r == 0.0f) return sd;
+  const int sr = r < 0.0f ? -1 : 1;
+  if (sd == sr) return sr;
+  const uint32_t rf = (__float_as_uint(r) >> 23) & 0xFFu;
+  if (rf == 0u) return 0;                                     // a subnormal r: leave it
+  const int32_t er = (int32_t)rf - 127, s = e2 - eref;        // |r| in [2^er, 2^(er + 1))
+  const int32_t eh = (int32_t)((__float_as_uint(hi) >> 23) & 0xFFu) - 127 + s;   // hi 2^s < 2^(eh + 1)
+  if (er > eh + 1) return sr;
+  if (sd != 0) {
+    const int32_t elo = (int32_t)((__float_as_uint(lo) >> 23) & 0xFFu) - 127 + s;  // lo 2^s >= 2^elo
+    if ((__float_as_uint(lo) & 0x7F800000u) != 0u && er + 1 < elo) return sd;
+  }
+  return 0;
+}
+
 // EXACT for BF16 and XF32 products (which fp32 cannot hold: they span 2^+-266 and
 // 2^+-254) on the FP32 pipe, with every term scaled by 2^-e_ref, e_ref = max(E_a + E_b,
 // e_c):
@@ -1273,8 +1334,8 @@ __device__ __forceinline__ int exact_fp32_round(float s, float E, float b, int r
 // the remainder, which no fixed bound gives).
 // The scaled result t' goes back by adding e_ref to its exponent field.  When that
 // reaches 2^128 the correctly rounded sum overflows: +-Inf under RNE, +-max-finite
-// under RTZ.  A subnormal result, a subnormal c and an undecided rounding return 2
-// (the integer path).  Inf/NaN operands and the CDNA 3 product-overflow rule are the
+// under RTZ.  A subnormal c scales up exactly when e_ref <= 0 and is dropped otherwise.
+// A subnormal result and an undecided rounding return 2 (the integer path).  Inf/NaN operands and the CDNA 3 product-overflow rule are the
 // caller's.  e_ref may exceed the largest nonzero product's exponent (a zero operand
 // counts with E = -126): that only moves terms toward the dropped range, and the bound
 // covers them.
@@ -1285,10 +1346,11 @@ __device__ __forceinline__ int exact_scaled(const uint32_t (&wa)[NW], const uint
   constexpr int32_t DMIN = ID == F_BF16 ? -110 : -104;
   constexpr float kDrop = ID == F_BF16 ? 0x1p-106f : 0x1p-100f;
   const uint32_t cf = (cb >> 23) & 0xFFu;
-  if (cf == 0u && (cb & 0x7FFFFFu) != 0u) return 2;        // subnormal c
+  const bool csub = cf == 0u && (cb & 0x7FFFFFu) != 0u;    // a subnormal c, exponent -126
+  const int32_t ce = cf ? (int32_t)cf - 127 : -126;
   float pp[K];
   int32_t el[K];
-  int32_t eref = cf ? (int32_t)cf - 127 : -1000;           // c = 0 takes no part
+  int32_t eref = (cf || csub) ? ce : -1000;                 // c = 0 takes no part
 #pragma unroll
   for (int l = 0; l < K; l++) {
     uint32_t xa, xb;                                        // the fp32 bits of a and b
@@ -1309,13 +1371,19 @@ __device__ __forceinline__ int exact_scaled(const uint32_t (&wa)[NW], const uint
   float bx = 0.0f;                                          // bound of the dropped terms
   uint32_t dsg = 0u;                                        // their signs: bit 0 +, bit 1 -
   float sv = 0.0f;
+  bool cdrop = false;
   if (cf) {
-    if ((int32_t)cf - eref >= 1) {
-      sv = __uint_as_float(cb - ((uint32_t)eref << 23));
-    } else {
-      bx = 0x1p-125f;
-      dsg = (cb >> 31) + 1u;
-    }
+    if ((int32_t)cf - eref >= 1) sv = __uint_as_float(cb - ((uint32_t)eref << 23));
+    else cdrop = true;
+  } else if (csub) {
+    // a subnormal c scales up exactly (e_ref <= 0, so 2^-e_ref <= 2^126); with e_ref > 0
+    // it falls below 2^-126 and is dropped
+    if (eref <= 0) sv = __fmul_rn(__uint_as_float(cb), __uint_as_float((uint32_t)(127 - eref) << 23));
+    else cdrop = true;
+  }
+  if (cdrop) {
+    bx = 0x1p-125f;
+    dsg = (cb >> 31) + 1u;
   }
   float e[K];
 #pragma unroll
@@ -1369,6 +1437,12 @@ __device__ __forceinline__ int exact_scaled(const uint32_t (&wa)[NW], const uint
       // the dropped terms, below 2^-98 in all and under ulp(t) / 2 for |t| >= 2^-71,
       // decide alone (r = 0) or agree with r
       dir = ((tb >> 31) + 1u == dsg) ? 1 : -1;
+    } else if (fb == 0.0f && dsg != 0u && ef >= (56u << 23)) {
+      // S - t = r + (dropped terms) exactly: its sign from a second rescaled sum over the
+      // dropped terms, set against r
+      const int sd = dropped_sum_sign<ID, K>(pp, el, eref, cb, ce, cdrop, r);
+      if (sd == 0) return 2;
+      dir = (sd < 0) == ((tb >> 31) != 0u) ? 1 : -1;
     } else {
       return 2;
     }
