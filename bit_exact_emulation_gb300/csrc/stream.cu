@@ -392,10 +392,27 @@ __global__ void __launch_bounds__(256) block_generic_kernel(const __grid_constan
 // workloads and the hardware presets; everything else takes the generic kernel
 // ---------------------------------------------------------------------------
 static int grid_for(size_t n, const void *kernel) {
+  // resident blocks per SM and the SM count, looked up once per (device, kernel) and
+  // thread: a short launch is otherwise dominated by the queries
+  struct Entry {
+    const void *kernel;
+    int dev, sms, per_sm;
+  };
+  static thread_local Entry cache[64];
+  static thread_local int cached = 0;
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+  for (int i = 0; i < cached; i++)
+    if (cache[i].kernel == kernel && cache[i].dev == dev) {
+      sms = cache[i].sms;
+      per_sm = cache[i].per_sm;
+      break;
+    }
+  if (sms == 0) {
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+    if (cached < 64) cache[cached++] = Entry{kernel, dev, sms, per_sm};
+  }
   if (per_sm < 1) per_sm = 1;
   size_t want = (n + 255) / 256;
   size_t full = (size_t)sms * per_sm;              // one wave of resident blocks
