@@ -362,6 +362,17 @@ extern "C" size_t mcemu_block_fma_host_workspace(mcemu_model_t model) {
   return 2 * per;
 }
 
+// a host pointer the device can dereference as it is: page-locked host memory mapped into
+// the unified address space (the device pointer equals the host pointer)
+static bool host_mapped(const void *p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();                                // an unregistered pointer, on older runtimes
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost && at.devicePointer == p;
+}
+
 extern "C" int mcemu_block_fma_host(mcemu_model_t model, size_t n, const void *a, const void *b,
                                     const uint32_t *c, uint32_t *d, void *workspace, size_t ws_bytes,
                                     void *stream) {
@@ -372,8 +383,16 @@ extern "C" int mcemu_block_fma_host(mcemu_model_t model, size_t n, const void *a
   if (!aligned(workspace, 256)) return MCEMU_ERR_ALIGNMENT;
   const DevModel &m = model->m.dev;
   const size_t vec = (size_t)m.k * elem_bytes(model->m.desc.fmt_a);
+  cudaStream_t s0 = (cudaStream_t)stream;
+  // page-locked buffers mapped into the device's address space: the kernels stream them
+  // in place over the host link, which beats staging through the copy engines
+  if (host_mapped(a) && host_mapped(b) && host_mapped(c) && host_mapped(d)) {
+    const int st = launch_block_fma(m, n, a, b, c, d, s0);
+    if (st != MCEMU_OK) return st;
+    return cudaStreamSynchronize(s0) == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
+  }
   const size_t sa = (vec * kHostChunk + 255) & ~(size_t)255, sc = (4 * kHostChunk + 255) & ~(size_t)255;
-  cudaStream_t s0 = (cudaStream_t)stream, ss[2];
+  cudaStream_t ss[2];
   cudaEvent_t done[2];
   if (cudaStreamCreateWithFlags(&ss[0], cudaStreamNonBlocking) != cudaSuccess) return MCEMU_ERR_CUDA;
   if (cudaStreamCreateWithFlags(&ss[1], cudaStreamNonBlocking) != cudaSuccess) {

@@ -163,9 +163,11 @@ int mcemu_model_get_desc(mcemu_model_t model, mcemu_model_desc *out);
  * alignment gives the vectorised path).  n = 0 is a no-op. */
 int mcemu_block_fma(mcemu_model_t model, size_t n, const void *a, const void *b,
                     const uint32_t *c, uint32_t *d, void *stream);
-/* The same from host memory: a, b, c and d are HOST buffers (pinned memory
- * overlaps best).  The library streams them through the caller's device
- * workspace in chunks, overlapping copies with compute on `stream`, and
+/* The same from host memory: a, b, c and d are HOST buffers.  When all four are
+ * page-locked and mapped into the device's address space (cudaHostAlloc memory
+ * under unified addressing), the kernels read and write them in place over the
+ * host link; otherwise the library streams them through the caller's device
+ * workspace in chunks, overlapping copies with compute.  Either way the call
  * returns after d has been written (synchronous).  ws_bytes must be at least
  * mcemu_block_fma_host_workspace(model, ...). */
 int mcemu_block_fma_host(mcemu_model_t model, size_t n, const void *a, const void *b,
