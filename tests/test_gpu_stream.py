@@ -397,6 +397,45 @@ def test_special_operand_mixes(L, fmt, k):
             assert np.array_equal(got, want), f"{fmt} {name} {out_round}\n" + mismatches(got, want, a, b, c)
 
 
+def _dropped_mix(fmt, n, k, seed):
+    """c in a high binade, at most one product within 30 binades of it (so the kept sum
+    leaves a remainder or none), the other products 112-140 binades below c with random
+    signs and nearby exponents: the sign of the dropped terms' sum decides RZ."""
+    rng = np.random.default_rng(seed)
+    mb = 7 if fmt == "bf16" else 23
+    dt = np.uint16 if fmt == "bf16" else np.uint32
+
+    def elem(field, size):
+        m = rng.integers(0, 1 << mb, size)
+        if fmt == "xf32":
+            m &= ~((1 << 13) - 1)
+        return ((rng.integers(0, 2, size) << (mb + 8)) | (np.clip(field, 1, 254) << mb) | m).astype(dt)
+
+    fc = rng.integers(150, 250, n)
+    # product field sums: the first near c (or far below it), the rest 112-140 binades down
+    gap = rng.integers(112, 141, (n, k))
+    gap[:, 0] = np.where(rng.random(n) < 0.5, rng.integers(1, 30, n), gap[:, 0])
+    gap[:, 1:] = np.minimum(gap[:, 1:], gap[:, 1:2] + rng.integers(0, 3, (n, k - 1)))   # nearby exponents
+    s = fc[:, None] + 127 - gap
+    fa = np.clip(s // 2, 1, 254)
+    fb = np.clip(s - fa, 1, 254)
+    a, b = elem(fa, (n, k)), elem(fb, (n, k))
+    c = ((rng.integers(0, 2, n) << 31) | (fc << 23) | rng.integers(0, 1 << 23, n)).astype(np.uint32)
+    return a, b, c
+
+
+@pytest.mark.parametrize("fmt,k", [("bf16", 4), ("xf32", 2)])
+def test_exact_rz_dropped_terms(L, fmt, k):
+    """Exact-then-round, RZ and RNE, where the rounding hinges on terms far below the kept
+    sum: their sign alone, or set against a small remainder of the kept sum."""
+    a, b, c = _dropped_mix(fmt, 60000, k, seed=89)
+    for out_round in ("rtz", "rne"):
+        spec = dict(block_models(fmt, k)["ieee_exact"], out_round=out_round)
+        got = gpu_block(L, spec, a, b, c)
+        want = oracle.block_fma_parallel(spec, a, b, c, threads=8)
+        assert np.array_equal(got, want), f"{fmt} {out_round}\n" + mismatches(got, want, a, b, c)
+
+
 @pytest.mark.parametrize("fmt,k", [("bf16", 4), ("xf32", 2)])
 def test_exact_scale_extremes(L, fmt, k):
     """Exact-then-round, RNE and RTZ, on BF16/XF32 sets at the ends of the exponent range,
