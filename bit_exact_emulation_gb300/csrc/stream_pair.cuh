@@ -259,7 +259,7 @@ __device__ __forceinline__ uint32_t pair_general(const DevModel &m, const uint32
 template <int ID, int RM> struct GaPairEv {
   static constexpr bool kSpecialQueue = true, kSlowQueue = false, kTable = false;
   static constexpr size_t kTableBytes = 0;
-  static constexpr int kThreads = kPairThreads;
+  static constexpr int kThreads = kPairThreads, kMinBlocks = 0;
   static __device__ __forceinline__ const void *table() { return nullptr; }
   static __device__ __forceinline__ uint32_t eval(const DevModel &, const GaPairK &k, const uint16_t *, const uint32_t (&wa)[2],
                                                   const uint32_t (&wb)[2], uint32_t cb, uint32_t &flag) {
@@ -394,7 +394,7 @@ __device__ __forceinline__ int sigma_exact_rn(const uint32_t (&wa)[2], const uin
 template <int ID, int RM> struct ExactPairEv {
   static constexpr bool kSpecialQueue = ID == F_XF32T || (ID == F_BF16 && RM == 0), kSlowQueue = true, kTable = false;
   static constexpr size_t kTableBytes = 0;
-  static constexpr int kThreads = kPairThreads;
+  static constexpr int kThreads = kPairThreads, kMinBlocks = 0;
   static __device__ __forceinline__ const void *table() { return nullptr; }
   static __device__ __forceinline__ uint32_t eval(const DevModel &m, const GaPairK &, const uint16_t *, const uint32_t (&wa)[2],
                                                   const uint32_t (&wb)[2], uint32_t cb, uint32_t &flag) {
@@ -484,9 +484,10 @@ __device__ __forceinline__ void pair_drain(PairQueue q, int qn, int lane, uint32
 }
 
 // Ev::kTable: the evaluator reads a lookup table of Ev::kTableBytes, which every CTA
-// copies from global into dynamic shared memory first.
+// copies from global into dynamic shared memory first.  Ev::kMinBlocks: the CTAs per
+// SM the register budget is sized for (0 leaves it to the compiler).
 template <class Ev>
-__global__ void __launch_bounds__(Ev::kThreads) pair_kernel(const __grid_constant__ DevModel m, uint32_t npairs,
+__global__ void __launch_bounds__(Ev::kThreads, Ev::kMinBlocks) pair_kernel(const __grid_constant__ DevModel m, uint32_t npairs,
                                                             const uint4 *__restrict__ a, const uint4 *__restrict__ b,
                                                             const uint2 *__restrict__ c, uint2 *__restrict__ d,
                                                             const GaPairK k) {
