@@ -381,10 +381,10 @@ static int f8_run_pair(const DevModel &m, size_t n, const void *a, const void *b
   return cudaGetLastError() == cudaSuccess ? MCEMU_OK : MCEMU_ERR_CUDA;
 }
 
-// The paired kernel takes OCP exact-then-round at K = 8 (the FP32-pipe evaluation) with
-// 16-byte-aligned operands and 8-byte-aligned c, d.  Global alignment keeps f8_kernel:
-// its product-table lookups want the occupancy of 512-thread CTAs (measured 5-7 %
-// slower in the paired kernel).
+// The paired kernel takes K = 8 sets with 16-byte-aligned operands and 8-byte-aligned
+// c, d: global alignment through the product table (512-thread CTAs), and OCP
+// exact-then-round on the FP32 pipe.  FNUZ exact-then-round, other block sizes and
+// unaligned buffers keep f8_kernel, one set per thread.
 template <int ID>
 static bool f8_pair_ok(const DevModel &m, size_t n, const void *a, const void *b, const uint32_t *c, const uint32_t *d) {
   if (m.k != 8 || n < 2 || n / 2 >= (1u << 31)) return false;
