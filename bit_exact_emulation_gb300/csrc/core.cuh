@@ -199,22 +199,6 @@ __device__ __forceinline__ bool hw_scale(float x, int32_t k, int rne, uint32_t &
   bits = __float_as_uint(y);
   return hw_normal(bits);
 }
-// The same with one multiply when 2^k is a normal float (the common case of the GEMM
-// merges; the stream kernels keep the branch-free two-multiply form).
-__device__ __forceinline__ bool hw_scale1(float x, int32_t k, int rne, uint32_t &bits) {
-  if ((uint32_t)(k + 126) <= 253u) {
-    const float s = __uint_as_float((uint32_t)(k + 127) << 23);
-    bits = __float_as_uint(rne ? __fmul_rn(x, s) : __fmul_rz(x, s));
-    return hw_normal(bits);
-  }
-  return hw_scale(x, k, rne, bits);
-}
-__device__ __forceinline__ bool hw_round32_1(int32_t S, int32_t k, int rne, uint32_t &bits) {
-  return hw_scale1(rne ? __int2float_rn(S) : __int2float_rz(S), k, rne, bits);
-}
-__device__ __forceinline__ bool hw_round64_1(int64_t S, int32_t k, int rne, uint32_t &bits) {
-  return hw_scale1(rne ? __ll2float_rn(S) : __ll2float_rz(S), k, rne, bits);
-}
 __device__ __forceinline__ bool hw_round32(int32_t S, int32_t k, int rne, uint32_t &bits) {
   return hw_scale(rne ? __int2float_rn(S) : __int2float_rz(S), k, rne, bits);
 }
