@@ -7,7 +7,6 @@
 """
 import ctypes
 import ctypes.util
-import itertools
 from fractions import Fraction
 
 import numpy as np

@@ -6,7 +6,6 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle.presets import PRESETS
 from bit_exact_emulation_gb300 import workloads as W
 from _golden import GOLDEN
 
