@@ -355,9 +355,9 @@ def _special_mix(fmt, n, k, seed):
     random bits (an Inf next to a tiny element while other products are huge, Inf * 0,
     Inf - Inf, NaN among huge terms), c likewise."""
     rng = np.random.default_rng(seed)
-    mb = {"bf16": 7, "fp16": 10, "xf32": 23}[fmt]
-    eb = 5 if fmt == "fp16" else 8
-    dt = np.uint32 if fmt == "xf32" else np.uint16
+    mb = {"bf16": 7, "fp16": 10, "xf32": 23, "e4m3": 3, "e5m2": 2}[fmt]
+    eb = {"fp16": 5, "e4m3": 4, "e5m2": 5}.get(fmt, 8)
+    dt = {"xf32": np.uint32, "e4m3": np.uint8, "e5m2": np.uint8}.get(fmt, np.uint16)
     emax = (1 << eb) - 1
 
     def draw(shape, mbits, ebits):
@@ -383,11 +383,14 @@ def _special_mix(fmt, n, k, seed):
     return a, b, c
 
 
-@pytest.mark.parametrize("fmt,k", [("bf16", 4), ("xf32", 2), ("fp16", 4)])
+@pytest.mark.parametrize("fmt,k", [("bf16", 4), ("xf32", 2), ("fp16", 4), ("e4m3", 8), ("e5m2", 8)])
 def test_special_operand_mixes(L, fmt, k):
     """Every stream model on sets dense in Inf, NaN, zeros and extreme binades: the
     special result (NaN for a NaN, Inf * 0 or Inf - Inf, else the signed Inf) and the
-    finite results around them."""
+    finite results around them.  OCP FP8 at K = 8 runs the paired kernel's product
+    table, whose special entries (and, for E5M2, the signs of infinite products)
+    decide these sets; E4M3's all-ones exponent field is finite but for the NaN
+    mantissa."""
     a, b, c = _special_mix(fmt, 50000, k, seed=97)
     for name, spec in block_models(fmt, k).items():
         for out_round in ("rne", "rtz") if name == "ieee_exact" else (None,):
