@@ -1,5 +1,8 @@
 """Emulated GEMMs on the GPU (dense tile GEMM, 2:4 compression and sparse GEMM,
 multi-word GEMM), bit for bit against the oracle through the C ABI."""
+import os
+import threading
+
 import numpy as np
 import pytest
 
@@ -239,18 +242,36 @@ def test_in_place_accumulation(L, name):
     assert np.array_equal(host_u32(dC), want)
 
 
+def entries_parallel(fn, ii, jj):
+    """fn(ii_part, jj_part) over the host's cores: the oracle's C calls release the GIL
+    and keep no state between calls."""
+    parts = np.array_split(np.arange(len(ii)), max(1, min(os.cpu_count() or 1, 32)))
+    out = [None] * len(parts)
+
+    def work(t):
+        out[t] = fn(ii[parts[t]], jj[parts[t]])
+
+    ts = [threading.Thread(target=work, args=(t,)) for t in range(len(parts))]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    return np.concatenate(out)
+
+
 def test_dense_bf16_2048_sampled(L):
-    """The dense BF16 GEMM workload: M = N = K = 2048, 32x32x8 bf16 tile semantics."""
+    """The dense BF16 GEMM workload: M = N = K = 2048, 32x32x8 bf16 tile semantics;
+    2048 sampled outputs per model against the oracle."""
     M = N = K = 2048
     A, Bt, C = W.gen_dense_bf16(M, N, K, seed=3)
     rng = np.random.default_rng(11)
-    ii = rng.integers(0, M, 192).astype(np.int32)
-    jj = rng.integers(0, N, 192).astype(np.int32)
+    ii = rng.integers(0, M, 2048).astype(np.int32)
+    jj = rng.integers(0, N, 2048).astype(np.int32)
     for spec in (PRESETS["cdna3_bf16"], block_models("bf16", 4)["ga_trunc"], block_models("bf16", 4)["ga_rne"],
                  block_models("bf16", 4)["ieee_exact"]):
         m = L.Model(spec)
         D = host_u32(L.tile_gemm(m, L.tile(0, 32, 32, 8, 4), dev(A), dev(Bt), dev(C)))
-        want = oracle.gemm_entries(spec, K, 8, A, Bt, C, ii, jj)
+        want = entries_parallel(lambda i, j: oracle.gemm_entries(spec, K, 8, A, Bt, C, i, j), ii, jj)
         assert np.array_equal(D[ii, jj], want)
 
 
@@ -362,10 +383,10 @@ def test_sparse_e4m3_4096_sampled(L, case):
     m = L.Model(spec)
     D = host_u32(L.sparse24_gemm(m, L.tile(1, 16, 16, 32, 8), Ac, meta, dev(Bt), dev(C)))
     rng = np.random.default_rng(12 + case)
-    ii = rng.integers(0, M, 128).astype(np.int32)
-    jj = rng.integers(0, N, 128).astype(np.int32)
+    ii = rng.integers(0, M, 2048).astype(np.int32)
+    jj = rng.integers(0, N, 2048).astype(np.int32)
     hAc, hmeta = Ac.cpu().numpy(), meta.cpu().numpy()
-    want = oracle.sparse24_entries(spec, K, 32, hAc, hmeta, Bt, C, ii, jj)
+    want = entries_parallel(lambda i, j: oracle.sparse24_entries(spec, K, 32, hAc, hmeta, Bt, C, i, j), ii, jj)
     assert np.array_equal(D[ii, jj], want)
 
 
@@ -415,11 +436,12 @@ def test_multiword_fp64_4096_sampled(L):
     m = L.Model(PRESETS["cdna3_bf16"])
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(Bt).cuda()
     rng = np.random.default_rng(13)
-    ii = rng.integers(0, M, 24).astype(np.int32)
-    jj = rng.integers(0, N, 24).astype(np.int32)
+    ii = rng.integers(0, M, 256).astype(np.int32)
+    jj = rng.integers(0, N, 256).astype(np.int32)
     for truncated in (False, True):
         D = L.multiword_gemm(m, L.tile(0, 32, 32, 8, 4), 3, truncated, dA, dB).cpu().numpy()
-        want = oracle.multiword_entries(PRESETS["cdna3_bf16"], 8, 3, truncated, A, Bt, ii, jj)
+        want = entries_parallel(
+            lambda i, j: oracle.multiword_entries(PRESETS["cdna3_bf16"], 8, 3, truncated, A, Bt, i, j), ii, jj)
         assert np.array_equal(D[ii, jj].view(np.uint64), want.view(np.uint64))
 
 
